@@ -1,0 +1,165 @@
+/*
+ * specverify - the verify round of lossless speculative decoding on one GPU.
+ *
+ * Each round the target model runs the anchor token plus m draft tokens
+ * through every linear layer in one pass (mlx-dspark wiki page,
+ * "Architecture"), so every projection is a skinny matmul of M = 1 + m rows
+ * (1 <= M <= 32; B requests stack their rows into one block) against affine
+ * group-quantized weights, and the round ends in an accept step.
+ *
+ * Conventions for every entry point:
+ *   - All array pointers are DEVICE pointers owned by the caller unless the
+ *     parameter says "host".  The library allocates no device memory; calls
+ *     that need scratch space take a caller-provided workspace whose size comes
+ *     from the matching *_workspace_bytes() query.  A workspace must be zero
+ *     filled once after allocation (e.g. cudaMemsetAsync); every successful
+ *     call leaves its counters at zero again.  Calls sharing one workspace
+ *     must be ordered on one stream.
+ *   - bf16 and fp16 values are passed as uint16_t bit patterns.
+ *   - Matrices are row-major; ld* is the row stride in elements.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the
+ *     legacy default stream).  Arguments are validated on the host before
+ *     anything is launched: a bad argument returns SV_EINVAL (SV_EUNSUPPORTED
+ *     for a valid but unimplemented case) and launches nothing.  A failed
+ *     launch returns SV_ECUDA with the CUDA error text in sv_last_error().
+ *   - Kernels never trap.  A bounded wait that runs out (about 2 s) records
+ *     an error bit in a device word that sv_device_error() reads; results of
+ *     that call are then undefined.
+ *   - Nothing aborts the process and no C++ exception crosses this boundary.
+ *
+ * Weight format (mlx-dspark wiki page, "Key techniques": the verify kernel
+ * works per weight group; group 64, affine 4-/8-bit codes, fp16 scale and
+ * bias per group):
+ *   wq     uint32 [N, K*bits/32]: weight (n, k) is the `bits`-wide field of word
+ *          n*(K*bits/32) + k/(32/bits) at bit offset (k % (32/bits))*bits,
+ *          least significant field first.
+ *   scales fp16 [N, K/64], biases fp16 [N, K/64];  w[n,k] = scale*code + bias.
+ *   Requirements: bits in {4, 8}, group == 64, K % 512 == 0, K <= 65536,
+ *   N >= 1, wq 16-byte aligned (the weight rows are streamed by the tensor
+ *   memory accelerator in 512-wide k chunks).
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SV_OK = 0,
+  SV_EINVAL = 1,        /* bad argument: null/misaligned pointer, bad size */
+  SV_EUNSUPPORTED = 2,  /* valid request this build does not implement */
+  SV_ECUDA = 3,         /* a CUDA runtime/driver call failed */
+  SV_ETIMEOUT = 4       /* a device-side bounded wait ran out (sv_device_error) */
+} sv_status;
+
+/* Static text for a status code. */
+const char* sv_status_string(int status);
+/* Detail of the last non-OK status returned on the calling thread. */
+const char* sv_last_error(void);
+/* Library version, major*10000 + minor*100 + patch. */
+int sv_version(void);
+/* Waits for the device, then reads and clears the device error word.
+ * Returns SV_OK if no kernel recorded an error, SV_ETIMEOUT otherwise (the
+ * raw bits go to *bits when bits != NULL), SV_ECUDA if the device call fails. */
+int sv_device_error(unsigned int* bits);
+
+/* ------------------------------------------------------------------ qmm ---
+ * Y[m, n] = sum_k X[m, k] * w[n, k] for one verify projection
+ * (PyPI page, "The Apple-Silicon speedup ceiling": verify cost is the
+ * quantized matmul over every linear layer; wiki page, "Key techniques":
+ * each weight group is dequantized once and reused across all M rows).
+ * Arithmetic: fp32 accumulation, output rounded to bf16 (nearest even).
+ *   x  bf16 [M, K] with row stride ldx >= K;  y  bf16 [M, N], stride ldy >= N.
+ *   residual (optional, may be NULL): bf16 [M, N] with stride ldr; when given,
+ *   y = bf16(residual + bf16(x*w^T)), and y may alias residual (in-place add).
+ * Workspace: sv_qmm_workspace_bytes(M, N, K, bits) bytes, 256-byte aligned.
+ * The result is bitwise reproducible for a given (shape, device). */
+size_t sv_qmm_workspace_bytes(int M, int N, int K, int bits);
+int sv_qmm_verify(const uint32_t* wq, const uint16_t* scales, const uint16_t* biases, int N, int K, int bits,
+                  int group, const uint16_t* x, int ldx, int M, uint16_t* y, int ldy, const uint16_t* residual,
+                  int ldr, void* workspace, size_t workspace_bytes, void* stream);
+
+/* -------------------------------------------------------------- lm_head ---
+ * The vocab head of the round with its row softmax statistics fused in
+ * (wiki page, "Architecture": the draft is compared against the target's own
+ * logits; "Design decisions": verification keeps the full head transform).
+ *   logits  fp32 [M, V], stride ldl >= V (no 16-bit rounding).
+ *   row_max fp32 [M], row_argmax int32 [M] (lowest index attaining the max),
+ *   row_sumexp fp32 [M] = sum_v exp((logits - row_max) / T), written only when
+ *   temperature > 0 (may be NULL when temperature == 0).  Any of the three
+ *   row outputs may be NULL to skip it.
+ * temperature >= 0; 0 means greedy.
+ * Workspace: sv_lm_head_workspace_bytes(M, V, K, bits). */
+size_t sv_lm_head_workspace_bytes(int M, int V, int K, int bits);
+int sv_lm_head_verify(const uint32_t* wq, const uint16_t* scales, const uint16_t* biases, int V, int K, int bits,
+                      int group, const uint16_t* x, int ldx, int M, float temperature, float* logits, int ldl,
+                      float* row_max, float* row_sumexp, int32_t* row_argmax, void* workspace,
+                      size_t workspace_bytes, void* stream);
+
+/* --------------------------------------------------------------- accept ---
+ * Accept step of one round (B = 1) or of B independent requests.
+ * Greedy (temperature == 0; wiki page, "Architecture"; hysenlabs review,
+ * "The Problem"): a = first i < m with draft[i] != argmax(logits[i]) (a = m if
+ * none); out_tokens = draft[0..a-1] followed by argmax(logits[a]); out_len = a+1.
+ * Sampled (temperature > 0; releases page, v0.0.2 "Highlights"): with
+ * p_i = softmax(logits[i] / T), draft i is accepted iff u[i] < p_i[d]/q_i[d]
+ * (q_i[d] == 0 accepts).  At the first rejection i the committed token is the
+ * smallest k whose cumulative residual max(0, p_i - q_i) (index order) exceeds
+ * u[m] times its total (a zero residual falls back to p_i); if all m drafts
+ * are accepted the bonus token is drawn the same way from p_m.
+ *   logits fp32 [m+1, V] (stride ldl); q fp32 [m, V] draft probabilities
+ *   (stride ldq; unused and may be NULL when T == 0); draft int32 [m] token ids
+ *   in [0, V); u fp32 [m+1] uniforms in [0, 1) (may be NULL when T == 0).
+ *   row_max, row_sumexp, row_argmax: the lm_head row outputs for these rows.
+ *   They may all be NULL, in which case the call computes them itself (one
+ *   more pass over the logits); they must all be given or all be NULL.
+ *   out_len int32 [1]; out_tokens int32 [m+1] (entries past out_len untouched).
+ * 0 <= m <= 31, 2 <= V <= 2^24.
+ * Workspace: sv_accept_workspace_bytes(B, max_rows), max_rows = total logits rows. */
+size_t sv_accept_workspace_bytes(int B, int max_rows);
+int sv_spec_accept(const float* logits, int ldl, const float* row_max, const float* row_sumexp,
+                   const int32_t* row_argmax, const float* q, int ldq, const int32_t* draft, int m, int V,
+                   float temperature, const float* u, int32_t* out_len, int32_t* out_tokens, void* workspace,
+                   size_t workspace_bytes, void* stream);
+/* Batched form (PyPI page, "Concurrent throughput": B requests share one
+ * forward, each accepts and rolls back on its own).  row_offsets is a HOST
+ * array int32 [B+1]: request b owns logits rows [row_offsets[b], row_offsets[b+1])
+ * (m_b + 1 rows, 0 <= m_b <= 31), the q and draft rows starting at
+ * row_offsets[b] - b (m_b of them), uniforms u[row_offsets[b] .. +m_b], and
+ * writes out_len[b] and out_tokens[row_offsets[b] .. +m_b].  1 <= B <= 256. */
+int sv_spec_accept_batched(int B, const int32_t* row_offsets, const float* logits, int ldl, const float* row_max,
+                           const float* row_sumexp, const int32_t* row_argmax, const float* q, int ldq,
+                           const int32_t* draft, int V, float temperature, const float* u, int32_t* out_len,
+                           int32_t* out_tokens, void* workspace, size_t workspace_bytes, void* stream);
+
+/* --------------------------------------------------------------- philox ---
+ * n uniforms in [0, 1) from Philox-4x32-10 (Salmon et al., SC'11): element i is
+ * word (offset+i) % 4 of Philox(counter = (b lo, b hi, subsequence lo,
+ * subsequence hi), key = (seed lo, seed hi)), b = (offset+i) / 4, mapped to
+ * (word >> 8) * 2^-24.  Independent requests use distinct subsequences.
+ *   out fp32 [n], n >= 0. */
+int sv_philox_uniforms(uint64_t seed, uint64_t subsequence, uint64_t offset, int n, float* out, void* stream);
+
+/* ----------------------------------------------------------------- glue ---
+ * Row-wise steps between projections of a dense block (the pages give no
+ * layer internals; these are the usual RMSNorm / residual / SwiGLU).  fp32
+ * arithmetic, bf16 storage, one rounding per output.
+ *   sv_rmsnorm:   y = x / sqrt(mean(x^2) + eps) * weight   (weight bf16 [H] or NULL = 1)
+ *   sv_residual_add: h = h + t
+ *   sv_swiglu:    s = silu(g) * u,  silu(g) = g / (1 + exp(-g))
+ * M <= 4096 rows, H (or I) >= 1. */
+int sv_rmsnorm(const uint16_t* x, int ldx, int M, int H, const uint16_t* weight, float eps, uint16_t* y, int ldy,
+               void* stream);
+int sv_residual_add(uint16_t* h, int ldh, const uint16_t* t, int ldt, int M, int H, void* stream);
+int sv_swiglu(const uint16_t* g, int ldg, const uint16_t* u, int ldu, int M, int I, uint16_t* s, int lds,
+              void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECVERIFY_H */

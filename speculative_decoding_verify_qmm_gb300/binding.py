@@ -1,0 +1,238 @@
+"""ctypes binding of libspecverify with the same entry-point names as the C ABI.
+
+Argument marshalling only: every step runs in the library's CUDA kernels.
+Tensors are torch CUDA tensors (torch provides device memory and streams):
+
+* ``wq``      int32 [N, K*bits/32]  (uint32 words reinterpreted)
+* ``scales``  float16 [N, K/64],  ``biases`` float16 [N, K/64]
+* activations bfloat16, logits / probabilities float32, tokens int32
+
+Each call raises ``SVError`` when the library returns a non-OK status.  There
+is no fallback: if the shared library is missing or the tensors are not on a
+CUDA device the call fails.
+"""
+
+import ctypes
+import os
+import re
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libspecverify.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "specverify.h")
+
+SV_OK, SV_EINVAL, SV_EUNSUPPORTED, SV_ECUDA, SV_ETIMEOUT = range(5)
+
+_c_void_p, _c_int, _c_size_t, _c_float, _c_u64 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t,
+                                                  ctypes.c_float, ctypes.c_uint64)
+_c_uint_p = ctypes.POINTER(ctypes.c_uint)
+_c_i32_p = ctypes.POINTER(ctypes.c_int32)
+
+_SIGNATURES = {
+    "sv_status_string": (ctypes.c_char_p, [_c_int]),
+    "sv_last_error": (ctypes.c_char_p, []),
+    "sv_version": (_c_int, []),
+    "sv_device_error": (_c_int, [_c_uint_p]),
+    "sv_qmm_workspace_bytes": (_c_size_t, [_c_int, _c_int, _c_int, _c_int]),
+    "sv_qmm_verify": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_int, _c_int, _c_int, _c_int, _c_void_p, _c_int,
+                               _c_int, _c_void_p, _c_int, _c_void_p, _c_int, _c_void_p, _c_size_t, _c_void_p]),
+    "sv_lm_head_workspace_bytes": (_c_size_t, [_c_int, _c_int, _c_int, _c_int]),
+    "sv_lm_head_verify": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_int, _c_int, _c_int, _c_int, _c_void_p,
+                                   _c_int, _c_int, _c_float, _c_void_p, _c_int, _c_void_p, _c_void_p, _c_void_p,
+                                   _c_void_p, _c_size_t, _c_void_p]),
+    "sv_accept_workspace_bytes": (_c_size_t, [_c_int, _c_int]),
+    "sv_spec_accept": (_c_int, [_c_void_p, _c_int, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_int, _c_void_p,
+                                _c_int, _c_int, _c_float, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_size_t,
+                                _c_void_p]),
+    "sv_spec_accept_batched": (_c_int, [_c_int, _c_i32_p, _c_void_p, _c_int, _c_void_p, _c_void_p, _c_void_p,
+                                        _c_void_p, _c_int, _c_void_p, _c_int, _c_float, _c_void_p, _c_void_p,
+                                        _c_void_p, _c_void_p, _c_size_t, _c_void_p]),
+    "sv_philox_uniforms": (_c_int, [_c_u64, _c_u64, _c_u64, _c_int, _c_void_p, _c_void_p]),
+    "sv_rmsnorm": (_c_int, [_c_void_p, _c_int, _c_int, _c_int, _c_void_p, _c_float, _c_void_p, _c_int, _c_void_p]),
+    "sv_residual_add": (_c_int, [_c_void_p, _c_int, _c_void_p, _c_int, _c_int, _c_int, _c_void_p]),
+    "sv_swiglu": (_c_int, [_c_void_p, _c_int, _c_void_p, _c_int, _c_int, _c_int, _c_void_p, _c_int, _c_void_p]),
+}
+
+
+class SVError(RuntimeError):
+    def __init__(self, status, detail):
+        super().__init__("%s (status %d): %s" % (_STATUS_NAMES.get(status, "?"), status, detail))
+        self.status = status
+
+
+_STATUS_NAMES = {0: "SV_OK", 1: "SV_EINVAL", 2: "SV_EUNSUPPORTED", 3: "SV_ECUDA", 4: "SV_ETIMEOUT"}
+
+
+def header_functions():
+    """Names of the functions declared in include/specverify.h."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^[A-Za-z_][\w\s\*]*?\b(sv_\w+)\s*\(", text, flags=re.M)))
+
+
+def load_library(path=LIB_PATH):
+    """dlopen the library and attach the argument types (no device work)."""
+    if not os.path.exists(path):
+        raise RuntimeError("libspecverify.so is not built (run __graft_entry__.build())")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+class Library:
+    """The loaded library plus tensor-level helpers named after the C calls."""
+
+    def __init__(self, path=LIB_PATH):
+        self.lib = load_library(path)
+
+    # -------------------------------------------------------------- plumbing
+    def check(self, status):
+        if status != SV_OK:
+            raise SVError(status, self.lib.sv_last_error().decode())
+
+    def device_error(self):
+        bits = ctypes.c_uint(0)
+        st = self.lib.sv_device_error(ctypes.byref(bits))
+        if st not in (SV_OK, SV_ETIMEOUT):
+            self.check(st)
+        return bits.value
+
+    @staticmethod
+    def workspace(nbytes, device="cuda"):
+        """A zero-filled, 256-byte aligned device buffer (torch allocates it)."""
+        import torch
+        return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+    # ------------------------------------------------------------------ qmm
+    def qmm_workspace_bytes(self, M, N, K, bits):
+        return self.lib.sv_qmm_workspace_bytes(M, N, K, bits)
+
+    def qmm_verify(self, wq, scales, biases, K, bits, x, y=None, residual=None, workspace=None, stream=None):
+        import torch
+        M, N = x.shape[0], wq.shape[0]
+        if y is None:
+            y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+        if workspace is None:
+            workspace = self.workspace(self.qmm_workspace_bytes(M, N, K, bits), x.device)
+        self.check(self.lib.sv_qmm_verify(
+            _ptr(wq), _ptr(scales), _ptr(biases), N, K, bits, 64, _ptr(x), x.stride(0), M, _ptr(y), y.stride(0),
+            _ptr(residual), residual.stride(0) if residual is not None else 0, _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _stream(stream)))
+        return y
+
+    # -------------------------------------------------------------- lm_head
+    def lm_head_workspace_bytes(self, M, V, K, bits):
+        return self.lib.sv_lm_head_workspace_bytes(M, V, K, bits)
+
+    def lm_head_verify(self, wq, scales, biases, K, bits, x, temperature, logits=None, stats=True, workspace=None,
+                       stream=None):
+        import torch
+        M, V = x.shape[0], wq.shape[0]
+        dev = x.device
+        if logits is None:
+            logits = torch.empty((M, V), dtype=torch.float32, device=dev)
+        row_max = row_sumexp = row_argmax = None
+        if stats:
+            row_max = torch.empty(M, dtype=torch.float32, device=dev)
+            row_sumexp = torch.zeros(M, dtype=torch.float32, device=dev)
+            row_argmax = torch.empty(M, dtype=torch.int32, device=dev)
+        if workspace is None:
+            workspace = self.workspace(self.lm_head_workspace_bytes(M, V, K, bits), dev)
+        self.check(self.lib.sv_lm_head_verify(
+            _ptr(wq), _ptr(scales), _ptr(biases), V, K, bits, 64, _ptr(x), x.stride(0), M, float(temperature),
+            _ptr(logits), logits.stride(0), _ptr(row_max), _ptr(row_sumexp), _ptr(row_argmax), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _stream(stream)))
+        return logits, row_max, row_sumexp, row_argmax
+
+    # --------------------------------------------------------------- accept
+    def accept_workspace_bytes(self, B, rows):
+        return self.lib.sv_accept_workspace_bytes(B, rows)
+
+    def spec_accept(self, logits, draft, temperature, q=None, u=None, stats=None, workspace=None, stream=None):
+        """stats: (row_max, row_sumexp, row_argmax) from lm_head_verify, or None."""
+        import torch
+        m = logits.shape[0] - 1
+        V = logits.shape[1]
+        dev = logits.device
+        out_len = torch.zeros(1, dtype=torch.int32, device=dev)
+        out_tokens = torch.full((m + 1,), -1, dtype=torch.int32, device=dev)
+        if workspace is None:
+            workspace = self.workspace(self.accept_workspace_bytes(1, m + 1), dev)
+        rmax, rsum, rarg = stats if stats is not None else (None, None, None)
+        self.check(self.lib.sv_spec_accept(
+            _ptr(logits), logits.stride(0), _ptr(rmax), _ptr(rsum), _ptr(rarg), _ptr(q),
+            q.stride(0) if q is not None else 0, _ptr(draft), m, V, float(temperature), _ptr(u), _ptr(out_len),
+            _ptr(out_tokens), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+        return out_len, out_tokens
+
+    def spec_accept_batched(self, row_offsets, logits, drafts, temperature, q=None, u=None, stats=None,
+                            workspace=None, stream=None):
+        import torch
+        B = len(row_offsets) - 1
+        rows = int(row_offsets[-1])
+        V = logits.shape[1]
+        dev = logits.device
+        offs = (ctypes.c_int32 * (B + 1))(*[int(v) for v in row_offsets])
+        out_len = torch.zeros(B, dtype=torch.int32, device=dev)
+        out_tokens = torch.full((rows,), -1, dtype=torch.int32, device=dev)
+        if workspace is None:
+            workspace = self.workspace(self.accept_workspace_bytes(B, rows), dev)
+        rmax, rsum, rarg = stats if stats is not None else (None, None, None)
+        self.check(self.lib.sv_spec_accept_batched(
+            B, offs, _ptr(logits), logits.stride(0), _ptr(rmax), _ptr(rsum), _ptr(rarg), _ptr(q),
+            q.stride(0) if q is not None else 0, _ptr(drafts), V, float(temperature), _ptr(u), _ptr(out_len),
+            _ptr(out_tokens), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+        return out_len, out_tokens
+
+    # --------------------------------------------------------------- philox
+    def philox_uniforms(self, seed, subsequence, offset, n, out=None, stream=None):
+        import torch
+        if out is None:
+            out = torch.empty(n, dtype=torch.float32, device="cuda")
+        self.check(self.lib.sv_philox_uniforms(seed, subsequence, offset, n, _ptr(out), _stream(stream)))
+        return out
+
+    # ----------------------------------------------------------------- glue
+    def rmsnorm(self, x, weight=None, eps=1e-6, y=None, stream=None):
+        import torch
+        if y is None:
+            y = torch.empty_like(x)
+        self.check(self.lib.sv_rmsnorm(_ptr(x), x.stride(0), x.shape[0], x.shape[1], _ptr(weight), eps, _ptr(y),
+                                       y.stride(0), _stream(stream)))
+        return y
+
+    def residual_add(self, h, t, stream=None):
+        self.check(self.lib.sv_residual_add(_ptr(h), h.stride(0), _ptr(t), t.stride(0), h.shape[0], h.shape[1],
+                                            _stream(stream)))
+        return h
+
+    def swiglu(self, g, u, s=None, stream=None):
+        import torch
+        if s is None:
+            s = torch.empty_like(g)
+        self.check(self.lib.sv_swiglu(_ptr(g), g.stride(0), _ptr(u), u.stride(0), g.shape[0], g.shape[1], _ptr(s),
+                                      s.stride(0), _stream(stream)))
+        return s
+
+
+_LIB = None
+
+
+def load():
+    """The process-wide Library; builds nothing and falls back to nothing."""
+    global _LIB
+    if _LIB is None:
+        _LIB = Library()
+    return _LIB

@@ -1,0 +1,424 @@
+// C entry points of libspecverify: argument validation, workspace layout,
+// tensor-map encoding and kernel dispatch.  Nothing here allocates device
+// memory and nothing throws across the boundary.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "sv_internal.h"
+#include "sv_kernels.h"
+#include "sv_ptx.cuh"
+
+namespace sv {
+
+cudaError_t launch_qmm_b4(int NT, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const QmmParams&,
+                          cudaStream_t);
+cudaError_t launch_qmm_b8(int NT, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const QmmParams&,
+                          cudaStream_t);
+
+cudaError_t launch_qmm(int bits, int NT, const CUtensorMap& tw, const CUtensorMap& ts, const CUtensorMap& tb,
+                       const QmmParams& p, cudaStream_t s) {
+  return bits == 8 ? launch_qmm_b8(NT, tw, ts, tb, p, s) : launch_qmm_b4(NT, tw, ts, tb, p, s);
+}
+
+static thread_local char g_last[512] = "";
+
+static int fail(int status, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last, sizeof(g_last), fmt, ap);
+  va_end(ap);
+  return status;
+}
+static int cuda_fail(cudaError_t e, const char* what) {
+  return fail(SV_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+static size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int device_sm_count() {
+  static std::mutex mu;
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+Schedule make_schedule(int N, int K, int grid_limit) {
+  Schedule s;
+  s.N = N;
+  s.K = K;
+  s.tiles_n = (N + BN - 1) / BN;
+  s.units_per_tile = K / KC;
+  s.total_units = s.tiles_n * s.units_per_tile;
+  s.grid = s.total_units < grid_limit ? s.total_units : grid_limit;
+  return s;
+}
+
+QmmWorkspace qmm_workspace_layout(int M, int N, int K, int grid, bool with_stats) {
+  const int MP = 8 * ((M + 7) / 8);
+  const size_t tiles = (size_t)((N + BN - 1) / BN);
+  QmmWorkspace w;
+  size_t off = 0;
+  w.counters = off;   off = align256(off + tiles * 4);
+  w.xp = off;         off = align256(off + (size_t)K * MP * 2);
+  w.xsum = off;       off = align256(off + (size_t)(K / GROUP) * MP * 4);
+  w.rowscale = off;   off = align256(off + (size_t)MP * 4);
+  w.partials = off;   off = align256(off + (size_t)grid * 2 * BN * MP * 4);
+  w.tile_stats = off; off = align256(off + (with_stats ? tiles * MP * 12 : 0));
+  w.total = off;
+  return w;
+}
+
+// ------------------------------------------------------------- tensor maps
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+static int encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t dim0, uint64_t dim1,
+                     uint64_t stride1, uint32_t box0, uint32_t box1, CUtensorMapSwizzle sw) {
+  auto fn = encode_fn();
+  if (!fn) return fail(SV_ECUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t dims[2] = {dim0, dim1};
+  const cuuint64_t strides[1] = {stride1};
+  const cuuint32_t box[2] = {box0, box1};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(SV_ECUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+  return SV_OK;
+}
+
+// Shared validation of a quantized weight + activation block.
+static int check_weight(const uint32_t* wq, const uint16_t* scales, const uint16_t* biases, int N, int K, int bits,
+                        int group, int M) {
+  if (!wq || !scales || !biases) return fail(SV_EINVAL, "weight pointers must be non-null");
+  if (bits != 4 && bits != 8) return fail(SV_EUNSUPPORTED, "bits must be 4 or 8 (got %d)", bits);
+  if (group != GROUP) return fail(SV_EUNSUPPORTED, "group size must be 64 (got %d)", group);
+  if (N < 1 || N > (1 << 24)) return fail(SV_EINVAL, "N out of range (got %d)", N);
+  if (K < 1 || K % GROUP) return fail(SV_EINVAL, "K must be a positive multiple of 64 (got %d)", K);
+  if (K % KC) return fail(SV_EUNSUPPORTED, "K must be a multiple of 512 (got %d)", K);
+  if (K > (1 << 20)) return fail(SV_EINVAL, "K too large (got %d)", K);
+  if (M < 1) return fail(SV_EINVAL, "M must be >= 1 (got %d)", M);
+  if (M > MAX_M) return fail(SV_EUNSUPPORTED, "M must be <= 32 (got %d)", M);
+  if (!aligned(wq, 16) || !aligned(scales, 16) || !aligned(biases, 16))
+    return fail(SV_EINVAL, "wq, scales and biases must be 16-byte aligned");
+  return SV_OK;
+}
+
+struct QmmCall {
+  CUtensorMap tw, ts, tb;
+  QmmParams p;
+};
+
+static int prepare_qmm(QmmCall& c, const uint32_t* wq, const uint16_t* scales, const uint16_t* biases, int N, int K,
+                       int bits, int M, void* ws, bool with_stats) {
+  const int sms = device_sm_count();
+  if (sms <= 0) return fail(SV_ECUDA, "no CUDA device");
+  const int row_bytes = K * bits / 8;
+  int st = encode_2d(&c.tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, (uint64_t)row_bytes, (uint64_t)N, (uint64_t)row_bytes,
+                     128, BN, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (st) return st;
+  st = encode_2d(&c.ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, scales, (uint64_t)(K / GROUP), (uint64_t)N,
+                 (uint64_t)(K / GROUP) * 2, GPS, BN, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (st) return st;
+  st = encode_2d(&c.tb, CU_TENSOR_MAP_DATA_TYPE_UINT16, biases, (uint64_t)(K / GROUP), (uint64_t)N,
+                 (uint64_t)(K / GROUP) * 2, GPS, BN, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (st) return st;
+  QmmParams& p = c.p;
+  memset(&p, 0, sizeof(p));
+  p.sch = make_schedule(N, K, sms);
+  p.M = M;
+  p.MP = 8 * ((M + 7) / 8);
+  const QmmWorkspace L = qmm_workspace_layout(M, N, K, p.sch.grid, with_stats);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  p.counters = reinterpret_cast<int*>(base + L.counters);
+  p.xp = reinterpret_cast<const __half*>(base + L.xp);
+  p.xsum = reinterpret_cast<const float*>(base + L.xsum);
+  p.rowscale = reinterpret_cast<const float*>(base + L.rowscale);
+  p.partials = reinterpret_cast<float*>(base + L.partials);
+  p.tile_stats = with_stats ? reinterpret_cast<float*>(base + L.tile_stats) : nullptr;
+  return SV_OK;
+}
+
+static int run_qmm(QmmCall& c, const uint16_t* x, int ldx, int bits, void* ws, cudaStream_t s) {
+  const QmmParams& p = c.p;
+  cudaError_t e = launch_prep(reinterpret_cast<const __nv_bfloat16*>(x), ldx, p.M, p.MP, p.sch.K, bits,
+                              const_cast<__half*>(p.xp), const_cast<float*>(p.xsum), const_cast<float*>(p.rowscale), s);
+  if (e != cudaSuccess) return cuda_fail(e, "prep launch");
+  e = launch_qmm(bits, p.MP / 8, c.tw, c.ts, c.tb, p, s);
+  if (e != cudaSuccess) return cuda_fail(e, "qmm launch");
+  (void)ws;
+  return SV_OK;
+}
+
+}  // namespace sv
+
+using namespace sv;
+
+extern "C" {
+
+const char* sv_status_string(int status) {
+  switch (status) {
+    case SV_OK: return "ok";
+    case SV_EINVAL: return "invalid argument";
+    case SV_EUNSUPPORTED: return "unsupported";
+    case SV_ECUDA: return "CUDA error";
+    case SV_ETIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+const char* sv_last_error(void) { return g_last; }
+
+int sv_version(void) { return 100; }
+
+int sv_device_error(unsigned int* bits) {
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  unsigned int v = 0;
+  e = read_and_clear_error_word(&v);
+  if (e != cudaSuccess) return cuda_fail(e, "read error word");
+  if (bits) *bits = v;
+  if (v) return fail(SV_ETIMEOUT, "device error bits 0x%x", v);
+  return SV_OK;
+}
+
+size_t sv_qmm_workspace_bytes(int M, int N, int K, int bits) {
+  if (M < 1 || M > MAX_M || N < 1 || K < KC || K % KC || (bits != 4 && bits != 8)) return 0;
+  const int sms = device_sm_count();
+  if (sms <= 0) return 0;
+  return qmm_workspace_layout(M, N, K, make_schedule(N, K, sms).grid, false).total;
+}
+
+int sv_qmm_verify(const uint32_t* wq, const uint16_t* scales, const uint16_t* biases, int N, int K, int bits,
+                  int group, const uint16_t* x, int ldx, int M, uint16_t* y, int ldy, const uint16_t* residual,
+                  int ldr, void* workspace, size_t workspace_bytes, void* stream) {
+  int st = check_weight(wq, scales, biases, N, K, bits, group, M);
+  if (st) return st;
+  if (!x || !y || !workspace) return fail(SV_EINVAL, "x, y and workspace must be non-null");
+  if (ldx < K || ldy < N) return fail(SV_EINVAL, "ldx must be >= K and ldy >= N");
+  if (residual && ldr < N) return fail(SV_EINVAL, "ldr must be >= N");
+  if (!aligned(x, 2) || !aligned(y, 2) || (residual && !aligned(residual, 2)))
+    return fail(SV_EINVAL, "x, y, residual must be 2-byte aligned");
+  if (!aligned(workspace, 256)) return fail(SV_EINVAL, "workspace must be 256-byte aligned");
+  const size_t need = sv_qmm_workspace_bytes(M, N, K, bits);
+  if (need == 0) return fail(SV_ECUDA, "no CUDA device");
+  if (workspace_bytes < need) return fail(SV_EINVAL, "workspace too small: %zu < %zu", workspace_bytes, need);
+  QmmCall c;
+  st = prepare_qmm(c, wq, scales, biases, N, K, bits, M, workspace, false);
+  if (st) return st;
+  c.p.mode = residual ? EPI_BF16_RESIDUAL : EPI_BF16;
+  c.p.y = reinterpret_cast<__nv_bfloat16*>(y);
+  c.p.ldy = ldy;
+  c.p.res = reinterpret_cast<const __nv_bfloat16*>(residual);
+  c.p.ldres = ldr;
+  return run_qmm(c, x, ldx, bits, workspace, static_cast<cudaStream_t>(stream));
+}
+
+size_t sv_lm_head_workspace_bytes(int M, int V, int K, int bits) {
+  if (M < 1 || M > MAX_M || V < 1 || K < KC || K % KC || (bits != 4 && bits != 8)) return 0;
+  const int sms = device_sm_count();
+  if (sms <= 0) return 0;
+  return qmm_workspace_layout(M, V, K, make_schedule(V, K, sms).grid, true).total;
+}
+
+int sv_lm_head_verify(const uint32_t* wq, const uint16_t* scales, const uint16_t* biases, int V, int K, int bits,
+                      int group, const uint16_t* x, int ldx, int M, float temperature, float* logits, int ldl,
+                      float* row_max, float* row_sumexp, int32_t* row_argmax, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  int st = check_weight(wq, scales, biases, V, K, bits, group, M);
+  if (st) return st;
+  if (!x || !logits || !workspace) return fail(SV_EINVAL, "x, logits and workspace must be non-null");
+  if (!(temperature >= 0.f) || std::isinf(temperature)) return fail(SV_EINVAL, "temperature must be finite and >= 0");
+  if (ldx < K || ldl < V) return fail(SV_EINVAL, "ldx must be >= K and ldl >= V");
+  if (!aligned(x, 2) || !aligned(logits, 4)) return fail(SV_EINVAL, "misaligned x or logits");
+  if (!aligned(workspace, 256)) return fail(SV_EINVAL, "workspace must be 256-byte aligned");
+  const size_t need = sv_lm_head_workspace_bytes(M, V, K, bits);
+  if (need == 0) return fail(SV_ECUDA, "no CUDA device");
+  if (workspace_bytes < need) return fail(SV_EINVAL, "workspace too small: %zu < %zu", workspace_bytes, need);
+  QmmCall c;
+  st = prepare_qmm(c, wq, scales, biases, V, K, bits, M, workspace, true);
+  if (st) return st;
+  c.p.mode = EPI_LOGITS;
+  c.p.logits = logits;
+  c.p.ldl = ldl;
+  c.p.inv_temp = temperature > 0.f ? 1.f / temperature : 0.f;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = run_qmm(c, x, ldx, bits, workspace, s);
+  if (st) return st;
+  if (row_max || row_sumexp || row_argmax) {
+    cudaError_t e = launch_lmhead_finalize(c.p.tile_stats, c.p.sch.tiles_n, c.p.MP, M, c.p.inv_temp, row_max,
+                                           row_sumexp, row_argmax, s);
+    if (e != cudaSuccess) return cuda_fail(e, "lm_head finalize launch");
+  }
+  return SV_OK;
+}
+
+// ---------------------------------------------------------------- accept
+static int accept_chunks(int V) {
+  int nb = V / 2048;
+  return nb < 1 ? 1 : (nb > 64 ? 64 : nb);
+}
+
+size_t sv_accept_workspace_bytes(int B, int max_rows) {
+  if (B < 1 || B > MAX_BATCH || max_rows < 1) return 0;
+  return align256((size_t)B * 4) + align256((size_t)B * 64 * 2 * 8) + align256((size_t)max_rows * 12);
+}
+
+int sv_spec_accept_batched(int B, const int32_t* row_offsets, const float* logits, int ldl, const float* row_max,
+                           const float* row_sumexp, const int32_t* row_argmax, const float* q, int ldq,
+                           const int32_t* draft, int V, float temperature, const float* u, int32_t* out_len,
+                           int32_t* out_tokens, void* workspace, size_t workspace_bytes, void* stream) {
+  if (B < 1 || B > MAX_BATCH) return fail(SV_EINVAL, "B must be in [1, 256] (got %d)", B);
+  if (!row_offsets) return fail(SV_EINVAL, "row_offsets must be non-null");
+  if (row_offsets[0] != 0) return fail(SV_EINVAL, "row_offsets[0] must be 0");
+  int max_m = 0;
+  for (int b = 0; b < B; ++b) {
+    const int mb = row_offsets[b + 1] - row_offsets[b] - 1;
+    if (mb < 0 || mb > 31) return fail(SV_EINVAL, "request %d has m = %d (must be in [0, 31])", b, mb);
+    max_m = mb > max_m ? mb : max_m;
+  }
+  const int rows = row_offsets[B];
+  if (V < 2 || V > (1 << 24)) return fail(SV_EINVAL, "V must be in [2, 2^24] (got %d)", V);
+  if (!(temperature >= 0.f) || std::isinf(temperature)) return fail(SV_EINVAL, "temperature must be finite and >= 0");
+  const bool sampled = temperature > 0.f;
+  if (!logits || !out_len || !out_tokens || !workspace) return fail(SV_EINVAL, "null pointer argument");
+  if (max_m > 0 && !draft) return fail(SV_EINVAL, "draft must be non-null when m > 0");
+  if (ldl < V) return fail(SV_EINVAL, "ldl must be >= V");
+  if (sampled && (!u || (max_m > 0 && !q))) return fail(SV_EINVAL, "sampled accept needs q and u");
+  if (sampled && max_m > 0 && ldq < V) return fail(SV_EINVAL, "ldq must be >= V");
+  const int given = (row_max != nullptr) + (row_sumexp != nullptr) + (row_argmax != nullptr);
+  const bool need_sumexp = sampled;
+  if (given != 0 && given != 3 && !(given == 2 && !need_sumexp && !row_sumexp))
+    return fail(SV_EINVAL, "row statistics must be all given or all NULL");
+  if (!aligned(workspace, 256)) return fail(SV_EINVAL, "workspace must be 256-byte aligned");
+  const size_t need = sv_accept_workspace_bytes(B, rows);
+  if (workspace_bytes < need) return fail(SV_EINVAL, "workspace too small: %zu < %zu", workspace_bytes, need);
+
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  const size_t off_sums = align256((size_t)B * 4);
+  const size_t off_stats = off_sums + align256((size_t)B * 64 * 2 * 8);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  AcceptParams p;
+  memset(&p, 0, sizeof(p));
+  for (int b = 0; b <= B; ++b) p.offs[b] = row_offsets[b];
+  p.logits = logits;
+  p.ldl = ldl;
+  if (given == 0) {
+    float* smax = reinterpret_cast<float*>(base + off_stats);
+    float* ssum = smax + rows;
+    int32_t* sarg = reinterpret_cast<int32_t*>(ssum + rows);
+    cudaError_t e = launch_row_stats(logits, ldl, rows, V, temperature, smax, ssum, sarg, s);
+    if (e != cudaSuccess) return cuda_fail(e, "row stats launch");
+    p.row_max = smax;
+    p.row_sumexp = ssum;
+    p.row_argmax = sarg;
+  } else {
+    p.row_max = row_max;
+    p.row_sumexp = row_sumexp;
+    p.row_argmax = row_argmax;
+  }
+  p.q = q;
+  p.ldq = ldq;
+  p.draft = draft;
+  p.V = V;
+  p.temperature = temperature;
+  p.u = u;
+  p.out_len = out_len;
+  p.out_tokens = out_tokens;
+  p.chunk_sums = reinterpret_cast<double*>(base + off_sums);
+  p.counters = reinterpret_cast<int*>(base);
+  p.nb = accept_chunks(V);
+  cudaError_t e = launch_accept(p, B, s);
+  if (e != cudaSuccess) return cuda_fail(e, "accept launch");
+  return SV_OK;
+}
+
+int sv_spec_accept(const float* logits, int ldl, const float* row_max, const float* row_sumexp,
+                   const int32_t* row_argmax, const float* q, int ldq, const int32_t* draft, int m, int V,
+                   float temperature, const float* u, int32_t* out_len, int32_t* out_tokens, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+  if (m < 0 || m > 31) return fail(SV_EINVAL, "m must be in [0, 31] (got %d)", m);
+  const int32_t offs[2] = {0, m + 1};
+  return sv_spec_accept_batched(1, offs, logits, ldl, row_max, row_sumexp, row_argmax, q, ldq, draft, V,
+                                temperature, u, out_len, out_tokens, workspace, workspace_bytes, stream);
+}
+
+// ---------------------------------------------------------------- philox
+int sv_philox_uniforms(uint64_t seed, uint64_t subsequence, uint64_t offset, int n, float* out, void* stream) {
+  if (n < 0) return fail(SV_EINVAL, "n must be >= 0");
+  if (n == 0) return SV_OK;
+  if (!out) return fail(SV_EINVAL, "out must be non-null");
+  cudaError_t e = launch_philox(seed, subsequence, offset, n, out, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "philox launch");
+  return SV_OK;
+}
+
+// ------------------------------------------------------------------ glue
+static int check_rows(int M, int H) {
+  if (M < 1 || M > 4096) return fail(SV_EINVAL, "M must be in [1, 4096] (got %d)", M);
+  if (H < 1) return fail(SV_EINVAL, "row length must be >= 1 (got %d)", H);
+  return SV_OK;
+}
+
+int sv_rmsnorm(const uint16_t* x, int ldx, int M, int H, const uint16_t* weight, float eps, uint16_t* y, int ldy,
+               void* stream) {
+  int st = check_rows(M, H);
+  if (st) return st;
+  if (!x || !y) return fail(SV_EINVAL, "x and y must be non-null");
+  if (ldx < H || ldy < H) return fail(SV_EINVAL, "strides must be >= H");
+  if (!(eps >= 0.f)) return fail(SV_EINVAL, "eps must be >= 0");
+  cudaError_t e = launch_rmsnorm(reinterpret_cast<const __nv_bfloat16*>(x), ldx, M, H,
+                                 reinterpret_cast<const __nv_bfloat16*>(weight), eps,
+                                 reinterpret_cast<__nv_bfloat16*>(y), ldy, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "rmsnorm launch");
+  return SV_OK;
+}
+
+int sv_residual_add(uint16_t* h, int ldh, const uint16_t* t, int ldt, int M, int H, void* stream) {
+  int st = check_rows(M, H);
+  if (st) return st;
+  if (!h || !t) return fail(SV_EINVAL, "h and t must be non-null");
+  if (ldh < H || ldt < H) return fail(SV_EINVAL, "strides must be >= H");
+  cudaError_t e = launch_residual(reinterpret_cast<__nv_bfloat16*>(h), ldh, reinterpret_cast<const __nv_bfloat16*>(t),
+                                  ldt, M, H, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "residual launch");
+  return SV_OK;
+}
+
+int sv_swiglu(const uint16_t* g, int ldg, const uint16_t* u, int ldu, int M, int I, uint16_t* s, int lds,
+              void* stream) {
+  int st = check_rows(M, I);
+  if (st) return st;
+  if (!g || !u || !s) return fail(SV_EINVAL, "g, u and s must be non-null");
+  if (ldg < I || ldu < I || lds < I) return fail(SV_EINVAL, "strides must be >= I");
+  cudaError_t e = launch_swiglu(reinterpret_cast<const __nv_bfloat16*>(g), ldg,
+                                reinterpret_cast<const __nv_bfloat16*>(u), ldu, M, I,
+                                reinterpret_cast<__nv_bfloat16*>(s), lds, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "swiglu launch");
+  return SV_OK;
+}
+
+}  // extern "C"

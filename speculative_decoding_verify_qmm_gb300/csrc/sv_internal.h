@@ -1,0 +1,71 @@
+// Internal interfaces between the C entry points and the kernel launchers.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/specverify.h"
+
+namespace sv {
+
+// ---------------------------------------------------------------- tiling
+constexpr int GROUP = 64;        // weights per quantization group (along K)
+constexpr int BN = 64;           // weight rows per CTA tile
+constexpr int KC = 512;          // k per pipeline stage (8 groups)
+constexpr int GPS = KC / GROUP;  // groups per stage
+constexpr int NCW = 4;           // consumer warps per CTA (each owns 2 groups of a stage)
+constexpr int QMM_THREADS = (NCW + 1) * 32;
+constexpr int MAX_M = 32;        // rows per verify block handled by the kernels
+
+enum EpiMode : int { EPI_BF16 = 0, EPI_BF16_RESIDUAL = 1, EPI_LOGITS = 2 };
+
+// Stream-K schedule shared by host and device.  Work unit = (tile, k-chunk):
+// units [c*total/grid, (c+1)*total/grid) belong to CTA c.
+struct Schedule {
+  int N, K, tiles_n, units_per_tile, total_units, grid;
+};
+
+struct QmmParams {
+  Schedule sch;
+  int M, MP;                       // rows, rows padded to the n8 MMA tile
+  // prepared activations (written by the prep kernel into the workspace)
+  const __half* xp;                // [K/32][MP][32] fp16, scaled by 2^e[m], permuted
+  const float* xsum;               // [K/64][MP] fp32, group sums of the scaled rows
+  const float* rowscale;           // [MP] 2^-e[m]
+  float* partials;                 // [grid][2][BN*MP]
+  int* counters;                   // [tiles_n], zero between calls
+  // epilogue
+  int mode;
+  __nv_bfloat16* y; int ldy;       // EPI_BF16 / EPI_BF16_RESIDUAL
+  const __nv_bfloat16* res; int ldres;
+  float* logits; int ldl;          // EPI_LOGITS
+  float* tile_stats;               // [tiles_n][MP][3] (max, argmax bits, sumexp)
+  float inv_temp;                  // 1/T, 0 for greedy
+};
+
+// Byte offsets of the pieces of a qmm workspace.
+struct QmmWorkspace {
+  size_t counters, xp, xsum, rowscale, partials, tile_stats, total;
+};
+
+Schedule make_schedule(int N, int K, int grid_limit);
+QmmWorkspace qmm_workspace_layout(int M, int N, int K, int grid, bool with_stats);
+int device_sm_count();
+cudaError_t read_and_clear_error_word(unsigned int* out);
+
+// Launchers (return cudaError_t of the launch).
+cudaError_t launch_prep(const __nv_bfloat16* x, int ldx, int M, int MP, int K, int bits, __half* xp,
+                        float* xsum, float* rowscale, cudaStream_t s);
+cudaError_t launch_qmm(int bits, int NT, const CUtensorMap& tw, const CUtensorMap& ts, const CUtensorMap& tb,
+                       const QmmParams& p, cudaStream_t s);
+cudaError_t launch_lmhead_finalize(const float* tile_stats, int tiles_n, int MP, int M, float inv_temp,
+                                   float* row_max, float* row_sumexp, int32_t* row_argmax, cudaStream_t s);
+
+// Common launch helper: programmatic-serialization attribute on every launch.
+cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, size_t smem, cudaStream_t s, cudaLaunchAttribute* attr);
+
+}  // namespace sv
