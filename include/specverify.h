@@ -11,10 +11,11 @@
  *   - All array pointers are DEVICE pointers owned by the caller unless the
  *     parameter says "host".  The library allocates no device memory; calls
  *     that need scratch space take a caller-provided workspace whose size comes
- *     from the matching *_workspace_bytes() query.  A workspace must be zero
- *     filled once after allocation (e.g. cudaMemsetAsync); every successful
- *     call leaves its counters at zero again.  Calls sharing one workspace
- *     must be ordered on one stream.
+ *     from the matching *_workspace_bytes() query, 256-byte aligned.  Every
+ *     workspace starts with a 256 KiB block of counters that must be zero
+ *     filled once after allocation (e.g. cudaMemsetAsync) and that every
+ *     successful call leaves at zero again, so one workspace (sized for the
+ *     largest call) can serve any sequence of calls ordered on one stream.
  *   - bf16 and fp16 values are passed as uint16_t bit patterns.
  *   - Matrices are row-major; ld* is the row stride in elements.
  *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the
@@ -34,8 +35,8 @@
  *          n*(K*bits/32) + k/(32/bits) at bit offset (k % (32/bits))*bits,
  *          least significant field first.
  *   scales fp16 [N, K/64], biases fp16 [N, K/64];  w[n,k] = scale*code + bias.
- *   Requirements: bits in {4, 8}, group == 64, K % 512 == 0, K <= 65536,
- *   N >= 1, wq 16-byte aligned (the weight rows are streamed by the tensor
+ *   Requirements: bits in {4, 8}, group == 64, K % 512 == 0, K <= 2^20,
+ *   1 <= N <= 2^22, wq, scales and biases 16-byte aligned (the weight rows are streamed by the tensor
  *   memory accelerator in 512-wide k chunks).
  */
 #ifndef SPECVERIFY_H
@@ -83,6 +84,24 @@ int sv_qmm_verify(const uint32_t* wq, const uint16_t* scales, const uint16_t* bi
                   int group, const uint16_t* x, int ldx, int M, uint16_t* y, int ldy, const uint16_t* residual,
                   int ldr, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Split form of sv_qmm_verify for chains of projections.  sv_qmm_prepare
+ * converts one activation block into the layout the matmul kernel streams
+ * (kept in the workspace); each later sv_qmm_run / sv_lm_head_run with the
+ * same M, K and bits consumes it, so several projections of one input
+ * share one preparation.  The preparation can fuse the step that produces
+ * the activations:
+ *   SV_PREP_PLAIN    x as given (bf16 [M, K], stride ldx)
+ *   SV_PREP_RMSNORM  bf16(x / sqrt(mean(x^2) + eps) * weight), weight bf16 [K] or NULL = 1
+ *   SV_PREP_SWIGLU   bf16(silu(x) * x2) with x2 bf16 [M, K] (stride ldx2)
+ * The fused results are bit-identical to sv_rmsnorm / sv_swiglu followed by
+ * SV_PREP_PLAIN.  Workspace: sv_qmm_workspace_bytes() of the run that follows. */
+enum { SV_PREP_PLAIN = 0, SV_PREP_RMSNORM = 1, SV_PREP_SWIGLU = 2 };
+int sv_qmm_prepare(const uint16_t* x, int ldx, int M, int K, int bits, int mode, const uint16_t* x2, int ldx2,
+                   const uint16_t* rms_weight, float eps, void* workspace, size_t workspace_bytes, void* stream);
+int sv_qmm_run(const uint32_t* wq, const uint16_t* scales, const uint16_t* biases, int N, int K, int bits, int group,
+               int M, uint16_t* y, int ldy, const uint16_t* residual, int ldr, void* workspace,
+               size_t workspace_bytes, void* stream);
+
 /* -------------------------------------------------------------- lm_head ---
  * The vocab head of the round with its row softmax statistics fused in
  * (wiki page, "Architecture": the draft is compared against the target's own
@@ -99,6 +118,10 @@ int sv_lm_head_verify(const uint32_t* wq, const uint16_t* scales, const uint16_t
                       int group, const uint16_t* x, int ldx, int M, float temperature, float* logits, int ldl,
                       float* row_max, float* row_sumexp, int32_t* row_argmax, void* workspace,
                       size_t workspace_bytes, void* stream);
+/* The vocab head on activations prepared by sv_qmm_prepare (same M, K, bits). */
+int sv_lm_head_run(const uint32_t* wq, const uint16_t* scales, const uint16_t* biases, int V, int K, int bits,
+                   int group, int M, float temperature, float* logits, int ldl, float* row_max, float* row_sumexp,
+                   int32_t* row_argmax, void* workspace, size_t workspace_bytes, void* stream);
 
 /* --------------------------------------------------------------- accept ---
  * Accept step of one round (B = 1) or of B independent requests.
@@ -157,6 +180,59 @@ int sv_rmsnorm(const uint16_t* x, int ldx, int M, int H, const uint16_t* weight,
 int sv_residual_add(uint16_t* h, int ldh, const uint16_t* t, int ldt, int M, int H, void* stream);
 int sv_swiglu(const uint16_t* g, int ldg, const uint16_t* u, int ldu, int M, int I, uint16_t* s, int lds,
               void* stream);
+
+/* --------------------------------------------------------- verify round ---
+ * One whole verify round of a dense target whose every linear layer is
+ * group-quantized (wiki page, "Architecture": the target runs [anchor] + m
+ * drafts in one forward, then the accept step; PyPI page, "The Apple-Silicon
+ * speedup ceiling": verify cost is the quantized matmul over every layer).
+ * The pages give no layer internals; the body used here is
+ *   h += o(q(RMSNorm(h)))                       (q feeds o: no attention state)
+ *   h += down(silu(gate(a)) * up(a)),  a = RMSNorm(h)
+ * with RMSNorm weight 1.0 and k, v computed alongside q and unused, followed
+ * by a = RMSNorm(h), the vocab head (sv_lm_head_run) and the accept step
+ * (sv_spec_accept_batched semantics).  All weights use model->bits, group 64.
+ *
+ * sv_qweight: one quantized matrix [N, K] in the format above (device pointers).
+ * sv_layer:   qkv  = q | k | v stacked along N (first q_dim rows are q), K = hidden
+ *             o    = [hidden, q_dim]
+ *             gate_up = gate | up stacked along N (inter rows each), K = hidden
+ *             down = [hidden, inter]
+ * sv_model:   `layers` is a HOST array of n_layers entries; every layer's qkv
+ *             has the same N; lm_head = [vocab, hidden].
+ *
+ * sv_verify_round enqueues the whole round (8 launches per layer plus 4) on
+ * `stream`; it can be captured into a CUDA graph.  Arguments:
+ *   B, row_offsets (HOST int32 [B+1]): requests stacked into M = row_offsets[B]
+ *     rows, 1 <= M <= 32, each as in sv_spec_accept_batched.
+ *   hidden  bf16 [M, hidden] (stride ldh): the rows' input hidden states;
+ *     updated in place to the final residual stream.
+ *   temperature, q (fp32, stride ldq), draft (int32), u (fp32): as in
+ *     sv_spec_accept_batched.
+ *   logits  fp32 [M, vocab] (stride ldl): the round's target logits.
+ *   out_len int32 [B], out_tokens int32 [M]: the accept result.
+ * Workspace: sv_round_workspace_bytes(model, M) bytes (zero prefix rule above). */
+typedef struct {
+  const uint32_t* wq;
+  const uint16_t* scales;
+  const uint16_t* biases;
+  int N, K;
+} sv_qweight;
+typedef struct {
+  sv_qweight qkv, o, gate_up, down;
+} sv_layer;
+typedef struct {
+  int n_layers, hidden, q_dim, inter, vocab, bits;
+  float rms_eps;
+  const sv_layer* layers;
+  sv_qweight lm_head;
+} sv_model;
+
+size_t sv_round_workspace_bytes(const sv_model* model, int rows);
+int sv_verify_round(const sv_model* model, int B, const int32_t* row_offsets, uint16_t* hidden, int ldh,
+                    float temperature, const float* q, int ldq, const int32_t* draft, const float* u, float* logits,
+                    int ldl, int32_t* out_len, int32_t* out_tokens, void* workspace, size_t workspace_bytes,
+                    void* stream);
 
 #ifdef __cplusplus
 }

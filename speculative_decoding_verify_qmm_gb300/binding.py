@@ -27,6 +27,23 @@ _c_void_p, _c_int, _c_size_t, _c_float, _c_u64 = (ctypes.c_void_p, ctypes.c_int,
 _c_uint_p = ctypes.POINTER(ctypes.c_uint)
 _c_i32_p = ctypes.POINTER(ctypes.c_int32)
 
+class QWeight(ctypes.Structure):
+    _fields_ = [("wq", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("biases", ctypes.c_void_p),
+                ("N", ctypes.c_int), ("K", ctypes.c_int)]
+
+
+class Layer(ctypes.Structure):
+    _fields_ = [("qkv", QWeight), ("o", QWeight), ("gate_up", QWeight), ("down", QWeight)]
+
+
+class Model(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int), ("hidden", ctypes.c_int), ("q_dim", ctypes.c_int),
+                ("inter", ctypes.c_int), ("vocab", ctypes.c_int), ("bits", ctypes.c_int),
+                ("rms_eps", ctypes.c_float), ("layers", ctypes.POINTER(Layer)), ("lm_head", QWeight)]
+
+
+_c_model_p = ctypes.POINTER(Model)
+
 _SIGNATURES = {
     "sv_status_string": (ctypes.c_char_p, [_c_int]),
     "sv_last_error": (ctypes.c_char_p, []),
@@ -35,7 +52,18 @@ _SIGNATURES = {
     "sv_qmm_workspace_bytes": (_c_size_t, [_c_int, _c_int, _c_int, _c_int]),
     "sv_qmm_verify": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_int, _c_int, _c_int, _c_int, _c_void_p, _c_int,
                                _c_int, _c_void_p, _c_int, _c_void_p, _c_int, _c_void_p, _c_size_t, _c_void_p]),
+    "sv_qmm_prepare": (_c_int, [_c_void_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_void_p, _c_int, _c_void_p,
+                                _c_float, _c_void_p, _c_size_t, _c_void_p]),
+    "sv_qmm_run": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_void_p,
+                            _c_int, _c_void_p, _c_int, _c_void_p, _c_size_t, _c_void_p]),
     "sv_lm_head_workspace_bytes": (_c_size_t, [_c_int, _c_int, _c_int, _c_int]),
+    "sv_lm_head_run": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_float,
+                                _c_void_p, _c_int, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_size_t,
+                                _c_void_p]),
+    "sv_round_workspace_bytes": (_c_size_t, [_c_model_p, _c_int]),
+    "sv_verify_round": (_c_int, [_c_model_p, _c_int, _c_i32_p, _c_void_p, _c_int, _c_float, _c_void_p, _c_int,
+                                 _c_void_p, _c_void_p, _c_void_p, _c_int, _c_void_p, _c_void_p, _c_void_p,
+                                 _c_size_t, _c_void_p]),
     "sv_lm_head_verify": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_int, _c_int, _c_int, _c_int, _c_void_p,
                                    _c_int, _c_int, _c_float, _c_void_p, _c_int, _c_void_p, _c_void_p, _c_void_p,
                                    _c_void_p, _c_size_t, _c_void_p]),
@@ -132,6 +160,23 @@ class Library:
             workspace.numel() * workspace.element_size(), _stream(stream)))
         return y
 
+    def qmm_prepare(self, x, K, bits, mode=0, x2=None, rms_weight=None, eps=1e-6, workspace=None, stream=None):
+        M = x.shape[0]
+        self.check(self.lib.sv_qmm_prepare(
+            _ptr(x), x.stride(0), M, K, bits, mode, _ptr(x2), x2.stride(0) if x2 is not None else 0,
+            _ptr(rms_weight), eps, _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+    def qmm_run(self, wq, scales, biases, K, bits, M, y=None, residual=None, workspace=None, stream=None):
+        import torch
+        N = wq.shape[0]
+        if y is None:
+            y = torch.empty((M, N), dtype=torch.bfloat16, device=wq.device)
+        self.check(self.lib.sv_qmm_run(
+            _ptr(wq), _ptr(scales), _ptr(biases), N, K, bits, 64, M, _ptr(y), y.stride(0), _ptr(residual),
+            residual.stride(0) if residual is not None else 0, _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _stream(stream)))
+        return y
+
     # -------------------------------------------------------------- lm_head
     def lm_head_workspace_bytes(self, M, V, K, bits):
         return self.lib.sv_lm_head_workspace_bytes(M, V, K, bits)
@@ -155,6 +200,48 @@ class Library:
             _ptr(logits), logits.stride(0), _ptr(row_max), _ptr(row_sumexp), _ptr(row_argmax), _ptr(workspace),
             workspace.numel() * workspace.element_size(), _stream(stream)))
         return logits, row_max, row_sumexp, row_argmax
+
+    def lm_head_run(self, wq, scales, biases, K, bits, M, temperature, logits=None, stats=None, workspace=None,
+                    stream=None):
+        import torch
+        V = wq.shape[0]
+        if logits is None:
+            logits = torch.empty((M, V), dtype=torch.float32, device=wq.device)
+        rmax, rsum, rarg = stats if stats is not None else (None, None, None)
+        self.check(self.lib.sv_lm_head_run(
+            _ptr(wq), _ptr(scales), _ptr(biases), V, K, bits, 64, M, float(temperature), _ptr(logits),
+            logits.stride(0), _ptr(rmax), _ptr(rsum), _ptr(rarg), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _stream(stream)))
+        return logits
+
+    # ---------------------------------------------------------------- round
+    @staticmethod
+    def make_model(layers, lm_head, hidden, q_dim, inter, vocab, bits, rms_eps=1e-6):
+        """A ctypes sv_model over device weight dicts {'wq','scales','biases'} (kept alive by the caller).
+
+        ``layers``: list of dicts with keys qkv, o, gate_up, down."""
+        def qw(w):
+            return QWeight(w["wq"].data_ptr(), w["scales"].data_ptr(), w["biases"].data_ptr(), w["wq"].shape[0],
+                           w["K"])
+        arr = (Layer * len(layers))(*[Layer(qw(l["qkv"]), qw(l["o"]), qw(l["gate_up"]), qw(l["down"]))
+                                      for l in layers])
+        m = Model(len(layers), hidden, q_dim, inter, vocab, bits, rms_eps, arr, qw(lm_head))
+        # the struct holds raw device pointers: keep the tensors (and the array) alive with it
+        m._keep = (arr, layers, lm_head)
+        return m
+
+    def round_workspace_bytes(self, model, rows):
+        return self.lib.sv_round_workspace_bytes(ctypes.byref(model), rows)
+
+    def verify_round(self, model, row_offsets, hidden, temperature, logits, out_len, out_tokens, workspace,
+                     q=None, draft=None, u=None, stream=None):
+        B = len(row_offsets) - 1
+        offs = (ctypes.c_int32 * (B + 1))(*[int(v) for v in row_offsets])
+        self.check(self.lib.sv_verify_round(
+            ctypes.byref(model), B, offs, _ptr(hidden), hidden.stride(0), float(temperature), _ptr(q),
+            q.stride(0) if q is not None else 0, _ptr(draft), _ptr(u), _ptr(logits), logits.stride(0),
+            _ptr(out_len), _ptr(out_tokens), _ptr(workspace), workspace.numel() * workspace.element_size(),
+            _stream(stream)))
 
     # --------------------------------------------------------------- accept
     def accept_workspace_bytes(self, B, rows):

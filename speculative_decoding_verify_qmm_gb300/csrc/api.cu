@@ -27,19 +27,19 @@ cudaError_t launch_qmm(int bits, int NT, const CUtensorMap& tw, const CUtensorMa
 
 static thread_local char g_last[512] = "";
 
-static int fail(int status, const char* fmt, ...) {
+int fail(int status, const char* fmt, ...) {
   va_list ap;
   va_start(ap, fmt);
   vsnprintf(g_last, sizeof(g_last), fmt, ap);
   va_end(ap);
   return status;
 }
-static int cuda_fail(cudaError_t e, const char* what) {
+int cuda_fail(cudaError_t e, const char* what) {
   return fail(SV_ECUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
-static size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
-static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 int device_sm_count() {
   static std::mutex mu;
@@ -71,12 +71,13 @@ QmmWorkspace qmm_workspace_layout(int M, int N, int K, int grid, bool with_stats
   const size_t tiles = (size_t)((N + BN - 1) / BN);
   QmmWorkspace w;
   size_t off = 0;
-  w.counters = off;   off = align256(off + tiles * 4);
+  w.counters = 0;     off = COUNTER_BYTES;         // tiles <= MAX_TILES is checked by the callers
+  (void)tiles;
   w.xp = off;         off = align256(off + (size_t)K * MP * 2);
   w.xsum = off;       off = align256(off + (size_t)(K / GROUP) * MP * 4);
   w.rowscale = off;   off = align256(off + (size_t)MP * 4);
   w.partials = off;   off = align256(off + (size_t)grid * 2 * BN * MP * 4);
-  w.tile_stats = off; off = align256(off + (with_stats ? tiles * MP * 12 : 0));
+  w.tile_stats = off; off = align256(off + (with_stats ? (size_t)((N + BN - 1) / BN) * MP * 12 : 0));
   w.total = off;
   return w;
 }
@@ -111,12 +112,12 @@ static int encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base,
 }
 
 // Shared validation of a quantized weight + activation block.
-static int check_weight(const uint32_t* wq, const uint16_t* scales, const uint16_t* biases, int N, int K, int bits,
+int check_weight(const uint32_t* wq, const uint16_t* scales, const uint16_t* biases, int N, int K, int bits,
                         int group, int M) {
   if (!wq || !scales || !biases) return fail(SV_EINVAL, "weight pointers must be non-null");
   if (bits != 4 && bits != 8) return fail(SV_EUNSUPPORTED, "bits must be 4 or 8 (got %d)", bits);
   if (group != GROUP) return fail(SV_EUNSUPPORTED, "group size must be 64 (got %d)", group);
-  if (N < 1 || N > (1 << 24)) return fail(SV_EINVAL, "N out of range (got %d)", N);
+  if (N < 1 || N > MAX_TILES * BN) return fail(SV_EINVAL, "N out of range (got %d)", N);
   if (K < 1 || K % GROUP) return fail(SV_EINVAL, "K must be a positive multiple of 64 (got %d)", K);
   if (K % KC) return fail(SV_EUNSUPPORTED, "K must be a multiple of 512 (got %d)", K);
   if (K > (1 << 20)) return fail(SV_EINVAL, "K too large (got %d)", K);
@@ -162,15 +163,77 @@ static int prepare_qmm(QmmCall& c, const uint32_t* wq, const uint16_t* scales, c
   return SV_OK;
 }
 
-static int run_qmm(QmmCall& c, const uint16_t* x, int ldx, int bits, void* ws, cudaStream_t s) {
-  const QmmParams& p = c.p;
-  cudaError_t e = launch_prep(reinterpret_cast<const __nv_bfloat16*>(x), ldx, p.M, p.MP, p.sch.K, bits,
-                              const_cast<__half*>(p.xp), const_cast<float*>(p.xsum), const_cast<float*>(p.rowscale), s);
-  if (e != cudaSuccess) return cuda_fail(e, "prep launch");
-  e = launch_qmm(bits, p.MP / 8, c.tw, c.ts, c.tb, p, s);
-  if (e != cudaSuccess) return cuda_fail(e, "qmm launch");
-  (void)ws;
+// Validation of a prepare call (everything the host can check).
+static int check_prepare(const uint16_t* x, int ldx, int M, int K, int bits, int mode, const uint16_t* x2, int ldx2,
+                         void* ws) {
+  if (bits != 4 && bits != 8) return fail(SV_EUNSUPPORTED, "bits must be 4 or 8 (got %d)", bits);
+  if (K < 1 || K % GROUP) return fail(SV_EINVAL, "K must be a positive multiple of 64 (got %d)", K);
+  if (K % KC) return fail(SV_EUNSUPPORTED, "K must be a multiple of 512 (got %d)", K);
+  if (K > (1 << 20)) return fail(SV_EINVAL, "K too large (got %d)", K);
+  if (M < 1) return fail(SV_EINVAL, "M must be >= 1 (got %d)", M);
+  if (M > MAX_M) return fail(SV_EUNSUPPORTED, "M must be <= 32 (got %d)", M);
+  if (mode < PREP_PLAIN || mode > PREP_SWIGLU) return fail(SV_EINVAL, "unknown prepare mode %d", mode);
+  if (!x || !ws) return fail(SV_EINVAL, "x and workspace must be non-null");
+  if (ldx < K) return fail(SV_EINVAL, "ldx must be >= K");
+  if (mode == PREP_SWIGLU && (!x2 || ldx2 < K)) return fail(SV_EINVAL, "SwiGLU needs u with ldu >= K");
+  if (!aligned(ws, 256)) return fail(SV_EINVAL, "workspace must be 256-byte aligned");
   return SV_OK;
+}
+
+size_t prepare_bytes(int M, int K) { return qmm_workspace_layout(M, 1, K, 0, false).partials; }
+
+int qmm_prepare_internal(const uint16_t* x, int ldx, int M, int K, int bits, int mode, const uint16_t* x2, int ldx2,
+                         const uint16_t* w, float eps, void* ws, cudaStream_t s) {
+  const QmmWorkspace L = qmm_workspace_layout(M, 1, K, 0, false);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  PrepArgs a;
+  a.x = reinterpret_cast<const __nv_bfloat16*>(x);
+  a.ldx = ldx;
+  a.x2 = reinterpret_cast<const __nv_bfloat16*>(x2);
+  a.ldx2 = ldx2;
+  a.w = reinterpret_cast<const __nv_bfloat16*>(w);
+  a.eps = eps;
+  a.M = M;
+  a.MP = 8 * ((M + 7) / 8);
+  a.K = K;
+  a.xp = reinterpret_cast<__half*>(base + L.xp);
+  a.xsum = reinterpret_cast<float*>(base + L.xsum);
+  a.rowscale = reinterpret_cast<float*>(base + L.rowscale);
+  cudaError_t e = launch_prep(a, bits, mode, s);
+  if (e != cudaSuccess) return cuda_fail(e, "prepare launch");
+  return SV_OK;
+}
+
+int qmm_run_internal(const uint32_t* wq, const uint16_t* scales, const uint16_t* biases, int N, int K, int bits,
+                     int M, int mode, uint16_t* y, int ldy, const uint16_t* residual, int ldr, float* logits,
+                     int ldl, float temperature, float* row_max, float* row_sumexp, int32_t* row_argmax, void* ws,
+                     cudaStream_t s) {
+  QmmCall c;
+  const bool stats = mode == EPI_LOGITS;
+  int st = prepare_qmm(c, wq, scales, biases, N, K, bits, M, ws, stats);
+  if (st) return st;
+  c.p.mode = mode;
+  c.p.y = reinterpret_cast<__nv_bfloat16*>(y);
+  c.p.ldy = ldy;
+  c.p.res = reinterpret_cast<const __nv_bfloat16*>(residual);
+  c.p.ldres = ldr;
+  c.p.logits = logits;
+  c.p.ldl = ldl;
+  c.p.inv_temp = temperature > 0.f ? 1.f / temperature : 0.f;
+  cudaError_t e = launch_qmm(bits, c.p.MP / 8, c.tw, c.ts, c.tb, c.p, s);
+  if (e != cudaSuccess) return cuda_fail(e, "qmm launch");
+  if (stats && (row_max || row_sumexp || row_argmax)) {
+    e = launch_lmhead_finalize(c.p.tile_stats, c.p.sch.tiles_n, c.p.MP, M, c.p.inv_temp, row_max, row_sumexp,
+                               row_argmax, s);
+    if (e != cudaSuccess) return cuda_fail(e, "lm_head finalize launch");
+  }
+  return SV_OK;
+}
+
+size_t qmm_bytes(int M, int N, int K, bool stats) {
+  const int sms = device_sm_count();
+  if (sms <= 0) return 0;
+  return qmm_workspace_layout(M, N, K, make_schedule(N, K, sms).grid, stats).total;
 }
 
 }  // namespace sv
@@ -178,6 +241,109 @@ static int run_qmm(QmmCall& c, const uint16_t* x, int ldx, int bits, void* ws, c
 using namespace sv;
 
 extern "C" {
+
+size_t sv_qmm_workspace_bytes(int M, int N, int K, int bits) {
+  if (M < 1 || M > MAX_M || N < 1 || N > MAX_TILES * BN || K < KC || K % KC || (bits != 4 && bits != 8)) return 0;
+  return qmm_bytes(M, N, K, false);
+}
+
+size_t sv_lm_head_workspace_bytes(int M, int V, int K, int bits) {
+  if (M < 1 || M > MAX_M || V < 1 || V > MAX_TILES * BN || K < KC || K % KC || (bits != 4 && bits != 8)) return 0;
+  return qmm_bytes(M, V, K, true);
+}
+
+int sv_qmm_prepare(const uint16_t* x, int ldx, int M, int K, int bits, int mode, const uint16_t* x2, int ldx2,
+                   const uint16_t* rms_weight, float eps, void* workspace, size_t workspace_bytes, void* stream) {
+  int st = check_prepare(x, ldx, M, K, bits, mode, x2, ldx2, workspace);
+  if (st) return st;
+  if (mode == PREP_RMSNORM && !(eps >= 0.f)) return fail(SV_EINVAL, "eps must be >= 0");
+  if (workspace_bytes < prepare_bytes(M, K))
+    return fail(SV_EINVAL, "workspace too small: %zu < %zu", workspace_bytes, prepare_bytes(M, K));
+  return qmm_prepare_internal(x, ldx, M, K, bits, mode, x2, ldx2, rms_weight, eps, workspace,
+                              static_cast<cudaStream_t>(stream));
+}
+
+static int check_run(const uint32_t* wq, const uint16_t* scales, const uint16_t* biases, int N, int K, int bits,
+                     int group, int M, void* ws, size_t ws_bytes, bool stats) {
+  int st = check_weight(wq, scales, biases, N, K, bits, group, M);
+  if (st) return st;
+  if (!ws) return fail(SV_EINVAL, "workspace must be non-null");
+  if (!aligned(ws, 256)) return fail(SV_EINVAL, "workspace must be 256-byte aligned");
+  const size_t need = qmm_bytes(M, N, K, stats);
+  if (need == 0) return fail(SV_ECUDA, "no CUDA device");
+  if (ws_bytes < need) return fail(SV_EINVAL, "workspace too small: %zu < %zu", ws_bytes, need);
+  return SV_OK;
+}
+
+int sv_qmm_run(const uint32_t* wq, const uint16_t* scales, const uint16_t* biases, int N, int K, int bits, int group,
+               int M, uint16_t* y, int ldy, const uint16_t* residual, int ldr, void* workspace,
+               size_t workspace_bytes, void* stream) {
+  int st = check_run(wq, scales, biases, N, K, bits, group, M, workspace, workspace_bytes, false);
+  if (st) return st;
+  if (!y) return fail(SV_EINVAL, "y must be non-null");
+  if (ldy < N || (residual && ldr < N)) return fail(SV_EINVAL, "ldy and ldr must be >= N");
+  if (!aligned(y, 2) || (residual && !aligned(residual, 2))) return fail(SV_EINVAL, "misaligned y or residual");
+  return qmm_run_internal(wq, scales, biases, N, K, bits, M, residual ? EPI_BF16_RESIDUAL : EPI_BF16, y, ldy,
+                          residual, ldr, nullptr, 0, 0.f, nullptr, nullptr, nullptr, workspace,
+                          static_cast<cudaStream_t>(stream));
+}
+
+int sv_qmm_verify(const uint32_t* wq, const uint16_t* scales, const uint16_t* biases, int N, int K, int bits,
+                  int group, const uint16_t* x, int ldx, int M, uint16_t* y, int ldy, const uint16_t* residual,
+                  int ldr, void* workspace, size_t workspace_bytes, void* stream) {
+  int st = check_weight(wq, scales, biases, N, K, bits, group, M);
+  if (st) return st;
+  st = check_prepare(x, ldx, M, K, bits, PREP_PLAIN, nullptr, 0, workspace);
+  if (st) return st;
+  if (!y) return fail(SV_EINVAL, "y must be non-null");
+  if (ldy < N || (residual && ldr < N)) return fail(SV_EINVAL, "ldy and ldr must be >= N");
+  if (!aligned(y, 2) || (residual && !aligned(residual, 2))) return fail(SV_EINVAL, "misaligned y or residual");
+  st = check_run(wq, scales, biases, N, K, bits, group, M, workspace, workspace_bytes, false);
+  if (st) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = qmm_prepare_internal(x, ldx, M, K, bits, PREP_PLAIN, nullptr, 0, nullptr, 0.f, workspace, s);
+  if (st) return st;
+  return qmm_run_internal(wq, scales, biases, N, K, bits, M, residual ? EPI_BF16_RESIDUAL : EPI_BF16, y, ldy,
+                          residual, ldr, nullptr, 0, 0.f, nullptr, nullptr, nullptr, workspace, s);
+}
+
+static int check_head_outputs(float temperature, float* logits, int ldl, int V) {
+  if (!(temperature >= 0.f) || std::isinf(temperature)) return fail(SV_EINVAL, "temperature must be finite and >= 0");
+  if (!logits) return fail(SV_EINVAL, "logits must be non-null");
+  if (ldl < V) return fail(SV_EINVAL, "ldl must be >= V");
+  if (!aligned(logits, 4)) return fail(SV_EINVAL, "misaligned logits");
+  return SV_OK;
+}
+
+int sv_lm_head_run(const uint32_t* wq, const uint16_t* scales, const uint16_t* biases, int V, int K, int bits,
+                   int group, int M, float temperature, float* logits, int ldl, float* row_max, float* row_sumexp,
+                   int32_t* row_argmax, void* workspace, size_t workspace_bytes, void* stream) {
+  int st = check_run(wq, scales, biases, V, K, bits, group, M, workspace, workspace_bytes, true);
+  if (st) return st;
+  st = check_head_outputs(temperature, logits, ldl, V);
+  if (st) return st;
+  return qmm_run_internal(wq, scales, biases, V, K, bits, M, EPI_LOGITS, nullptr, 0, nullptr, 0, logits, ldl,
+                          temperature, row_max, row_sumexp, row_argmax, workspace, static_cast<cudaStream_t>(stream));
+}
+
+int sv_lm_head_verify(const uint32_t* wq, const uint16_t* scales, const uint16_t* biases, int V, int K, int bits,
+                      int group, const uint16_t* x, int ldx, int M, float temperature, float* logits, int ldl,
+                      float* row_max, float* row_sumexp, int32_t* row_argmax, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  int st = check_weight(wq, scales, biases, V, K, bits, group, M);
+  if (st) return st;
+  st = check_prepare(x, ldx, M, K, bits, PREP_PLAIN, nullptr, 0, workspace);
+  if (st) return st;
+  st = check_head_outputs(temperature, logits, ldl, V);
+  if (st) return st;
+  st = check_run(wq, scales, biases, V, K, bits, group, M, workspace, workspace_bytes, true);
+  if (st) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = qmm_prepare_internal(x, ldx, M, K, bits, PREP_PLAIN, nullptr, 0, nullptr, 0.f, workspace, s);
+  if (st) return st;
+  return qmm_run_internal(wq, scales, biases, V, K, bits, M, EPI_LOGITS, nullptr, 0, nullptr, 0, logits, ldl,
+                          temperature, row_max, row_sumexp, row_argmax, workspace, s);
+}
 
 const char* sv_status_string(int status) {
   switch (status) {
@@ -205,129 +371,36 @@ int sv_device_error(unsigned int* bits) {
   return SV_OK;
 }
 
-size_t sv_qmm_workspace_bytes(int M, int N, int K, int bits) {
-  if (M < 1 || M > MAX_M || N < 1 || K < KC || K % KC || (bits != 4 && bits != 8)) return 0;
-  const int sms = device_sm_count();
-  if (sms <= 0) return 0;
-  return qmm_workspace_layout(M, N, K, make_schedule(N, K, sms).grid, false).total;
-}
-
-int sv_qmm_verify(const uint32_t* wq, const uint16_t* scales, const uint16_t* biases, int N, int K, int bits,
-                  int group, const uint16_t* x, int ldx, int M, uint16_t* y, int ldy, const uint16_t* residual,
-                  int ldr, void* workspace, size_t workspace_bytes, void* stream) {
-  int st = check_weight(wq, scales, biases, N, K, bits, group, M);
-  if (st) return st;
-  if (!x || !y || !workspace) return fail(SV_EINVAL, "x, y and workspace must be non-null");
-  if (ldx < K || ldy < N) return fail(SV_EINVAL, "ldx must be >= K and ldy >= N");
-  if (residual && ldr < N) return fail(SV_EINVAL, "ldr must be >= N");
-  if (!aligned(x, 2) || !aligned(y, 2) || (residual && !aligned(residual, 2)))
-    return fail(SV_EINVAL, "x, y, residual must be 2-byte aligned");
-  if (!aligned(workspace, 256)) return fail(SV_EINVAL, "workspace must be 256-byte aligned");
-  const size_t need = sv_qmm_workspace_bytes(M, N, K, bits);
-  if (need == 0) return fail(SV_ECUDA, "no CUDA device");
-  if (workspace_bytes < need) return fail(SV_EINVAL, "workspace too small: %zu < %zu", workspace_bytes, need);
-  QmmCall c;
-  st = prepare_qmm(c, wq, scales, biases, N, K, bits, M, workspace, false);
-  if (st) return st;
-  c.p.mode = residual ? EPI_BF16_RESIDUAL : EPI_BF16;
-  c.p.y = reinterpret_cast<__nv_bfloat16*>(y);
-  c.p.ldy = ldy;
-  c.p.res = reinterpret_cast<const __nv_bfloat16*>(residual);
-  c.p.ldres = ldr;
-  return run_qmm(c, x, ldx, bits, workspace, static_cast<cudaStream_t>(stream));
-}
-
-size_t sv_lm_head_workspace_bytes(int M, int V, int K, int bits) {
-  if (M < 1 || M > MAX_M || V < 1 || K < KC || K % KC || (bits != 4 && bits != 8)) return 0;
-  const int sms = device_sm_count();
-  if (sms <= 0) return 0;
-  return qmm_workspace_layout(M, V, K, make_schedule(V, K, sms).grid, true).total;
-}
-
-int sv_lm_head_verify(const uint32_t* wq, const uint16_t* scales, const uint16_t* biases, int V, int K, int bits,
-                      int group, const uint16_t* x, int ldx, int M, float temperature, float* logits, int ldl,
-                      float* row_max, float* row_sumexp, int32_t* row_argmax, void* workspace,
-                      size_t workspace_bytes, void* stream) {
-  int st = check_weight(wq, scales, biases, V, K, bits, group, M);
-  if (st) return st;
-  if (!x || !logits || !workspace) return fail(SV_EINVAL, "x, logits and workspace must be non-null");
-  if (!(temperature >= 0.f) || std::isinf(temperature)) return fail(SV_EINVAL, "temperature must be finite and >= 0");
-  if (ldx < K || ldl < V) return fail(SV_EINVAL, "ldx must be >= K and ldl >= V");
-  if (!aligned(x, 2) || !aligned(logits, 4)) return fail(SV_EINVAL, "misaligned x or logits");
-  if (!aligned(workspace, 256)) return fail(SV_EINVAL, "workspace must be 256-byte aligned");
-  const size_t need = sv_lm_head_workspace_bytes(M, V, K, bits);
-  if (need == 0) return fail(SV_ECUDA, "no CUDA device");
-  if (workspace_bytes < need) return fail(SV_EINVAL, "workspace too small: %zu < %zu", workspace_bytes, need);
-  QmmCall c;
-  st = prepare_qmm(c, wq, scales, biases, V, K, bits, M, workspace, true);
-  if (st) return st;
-  c.p.mode = EPI_LOGITS;
-  c.p.logits = logits;
-  c.p.ldl = ldl;
-  c.p.inv_temp = temperature > 0.f ? 1.f / temperature : 0.f;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  st = run_qmm(c, x, ldx, bits, workspace, s);
-  if (st) return st;
-  if (row_max || row_sumexp || row_argmax) {
-    cudaError_t e = launch_lmhead_finalize(c.p.tile_stats, c.p.sch.tiles_n, c.p.MP, M, c.p.inv_temp, row_max,
-                                           row_sumexp, row_argmax, s);
-    if (e != cudaSuccess) return cuda_fail(e, "lm_head finalize launch");
-  }
-  return SV_OK;
-}
-
 // ---------------------------------------------------------------- accept
+}  // extern "C"
+
+namespace sv {
+
 static int accept_chunks(int V) {
   int nb = V / 2048;
   return nb < 1 ? 1 : (nb > 64 ? 64 : nb);
 }
 
-size_t sv_accept_workspace_bytes(int B, int max_rows) {
-  if (B < 1 || B > MAX_BATCH || max_rows < 1) return 0;
-  return align256((size_t)B * 4) + align256((size_t)B * 64 * 2 * 8) + align256((size_t)max_rows * 12);
-}
+// Accept scratch relative to the workspace base: per-request counters in the
+// zero prefix, chunk sums after it, then (only when the caller passes no row
+// statistics) the statistics of every row.
+static size_t accept_sums_offset() { return COUNTER_BYTES; }
+static size_t accept_stats_offset(int B) { return COUNTER_BYTES + align256((size_t)B * 64 * 2 * 8); }
+size_t accept_bytes(int B, int rows) { return accept_stats_offset(B) + align256((size_t)rows * 12); }
 
-int sv_spec_accept_batched(int B, const int32_t* row_offsets, const float* logits, int ldl, const float* row_max,
-                           const float* row_sumexp, const int32_t* row_argmax, const float* q, int ldq,
-                           const int32_t* draft, int V, float temperature, const float* u, int32_t* out_len,
-                           int32_t* out_tokens, void* workspace, size_t workspace_bytes, void* stream) {
-  if (B < 1 || B > MAX_BATCH) return fail(SV_EINVAL, "B must be in [1, 256] (got %d)", B);
-  if (!row_offsets) return fail(SV_EINVAL, "row_offsets must be non-null");
-  if (row_offsets[0] != 0) return fail(SV_EINVAL, "row_offsets[0] must be 0");
-  int max_m = 0;
-  for (int b = 0; b < B; ++b) {
-    const int mb = row_offsets[b + 1] - row_offsets[b] - 1;
-    if (mb < 0 || mb > 31) return fail(SV_EINVAL, "request %d has m = %d (must be in [0, 31])", b, mb);
-    max_m = mb > max_m ? mb : max_m;
-  }
-  const int rows = row_offsets[B];
-  if (V < 2 || V > (1 << 24)) return fail(SV_EINVAL, "V must be in [2, 2^24] (got %d)", V);
-  if (!(temperature >= 0.f) || std::isinf(temperature)) return fail(SV_EINVAL, "temperature must be finite and >= 0");
-  const bool sampled = temperature > 0.f;
-  if (!logits || !out_len || !out_tokens || !workspace) return fail(SV_EINVAL, "null pointer argument");
-  if (max_m > 0 && !draft) return fail(SV_EINVAL, "draft must be non-null when m > 0");
-  if (ldl < V) return fail(SV_EINVAL, "ldl must be >= V");
-  if (sampled && (!u || (max_m > 0 && !q))) return fail(SV_EINVAL, "sampled accept needs q and u");
-  if (sampled && max_m > 0 && ldq < V) return fail(SV_EINVAL, "ldq must be >= V");
-  const int given = (row_max != nullptr) + (row_sumexp != nullptr) + (row_argmax != nullptr);
-  const bool need_sumexp = sampled;
-  if (given != 0 && given != 3 && !(given == 2 && !need_sumexp && !row_sumexp))
-    return fail(SV_EINVAL, "row statistics must be all given or all NULL");
-  if (!aligned(workspace, 256)) return fail(SV_EINVAL, "workspace must be 256-byte aligned");
-  const size_t need = sv_accept_workspace_bytes(B, rows);
-  if (workspace_bytes < need) return fail(SV_EINVAL, "workspace too small: %zu < %zu", workspace_bytes, need);
-
-  uint8_t* base = static_cast<uint8_t*>(workspace);
-  const size_t off_sums = align256((size_t)B * 4);
-  const size_t off_stats = off_sums + align256((size_t)B * 64 * 2 * 8);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+int accept_internal(int B, const int32_t* offs, const float* logits, int ldl, const float* row_max,
+                    const float* row_sumexp, const int32_t* row_argmax, const float* q, int ldq, const int32_t* draft,
+                    int V, float temperature, const float* u, int32_t* out_len, int32_t* out_tokens, void* ws,
+                    cudaStream_t s) {
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  const int rows = offs[B];
   AcceptParams p;
   memset(&p, 0, sizeof(p));
-  for (int b = 0; b <= B; ++b) p.offs[b] = row_offsets[b];
+  for (int b = 0; b <= B; ++b) p.offs[b] = offs[b];
   p.logits = logits;
   p.ldl = ldl;
-  if (given == 0) {
-    float* smax = reinterpret_cast<float*>(base + off_stats);
+  if (!row_max && !row_argmax) {
+    float* smax = reinterpret_cast<float*>(base + accept_stats_offset(B));
     float* ssum = smax + rows;
     int32_t* sarg = reinterpret_cast<int32_t*>(ssum + rows);
     cudaError_t e = launch_row_stats(logits, ldl, rows, V, temperature, smax, ssum, sarg, s);
@@ -348,12 +421,62 @@ int sv_spec_accept_batched(int B, const int32_t* row_offsets, const float* logit
   p.u = u;
   p.out_len = out_len;
   p.out_tokens = out_tokens;
-  p.chunk_sums = reinterpret_cast<double*>(base + off_sums);
+  p.chunk_sums = reinterpret_cast<double*>(base + accept_sums_offset());
   p.counters = reinterpret_cast<int*>(base);
   p.nb = accept_chunks(V);
   cudaError_t e = launch_accept(p, B, s);
   if (e != cudaSuccess) return cuda_fail(e, "accept launch");
   return SV_OK;
+}
+
+int check_accept(int B, const int32_t* row_offsets, const float* logits, int ldl, const float* row_max,
+                 const float* row_sumexp, const int32_t* row_argmax, const float* q, int ldq, const int32_t* draft,
+                 int V, float temperature, const float* u, int32_t* out_len, int32_t* out_tokens) {
+  if (B < 1 || B > MAX_BATCH) return fail(SV_EINVAL, "B must be in [1, 256] (got %d)", B);
+  if (!row_offsets) return fail(SV_EINVAL, "row_offsets must be non-null");
+  if (row_offsets[0] != 0) return fail(SV_EINVAL, "row_offsets[0] must be 0");
+  int max_m = 0;
+  for (int b = 0; b < B; ++b) {
+    const int mb = row_offsets[b + 1] - row_offsets[b] - 1;
+    if (mb < 0 || mb > 31) return fail(SV_EINVAL, "request %d has m = %d (must be in [0, 31])", b, mb);
+    max_m = mb > max_m ? mb : max_m;
+  }
+  if (V < 2 || V > (1 << 24)) return fail(SV_EINVAL, "V must be in [2, 2^24] (got %d)", V);
+  if (!(temperature >= 0.f) || std::isinf(temperature)) return fail(SV_EINVAL, "temperature must be finite and >= 0");
+  const bool sampled = temperature > 0.f;
+  if (!logits || !out_len || !out_tokens) return fail(SV_EINVAL, "null pointer argument");
+  if (max_m > 0 && !draft) return fail(SV_EINVAL, "draft must be non-null when m > 0");
+  if (ldl < V) return fail(SV_EINVAL, "ldl must be >= V");
+  if (sampled && (!u || (max_m > 0 && !q))) return fail(SV_EINVAL, "sampled accept needs q and u");
+  if (sampled && max_m > 0 && ldq < V) return fail(SV_EINVAL, "ldq must be >= V");
+  const int given = (row_max != nullptr) + (row_sumexp != nullptr) + (row_argmax != nullptr);
+  const bool ok_stats = given == 0 || given == 3 || (!sampled && row_max && row_argmax && !row_sumexp);
+  if (!ok_stats) return fail(SV_EINVAL, "row statistics must be all given or all NULL");
+  return SV_OK;
+}
+
+}  // namespace sv
+
+extern "C" {
+
+size_t sv_accept_workspace_bytes(int B, int max_rows) {
+  if (B < 1 || B > MAX_BATCH || max_rows < 1) return 0;
+  return accept_bytes(B, max_rows);
+}
+
+int sv_spec_accept_batched(int B, const int32_t* row_offsets, const float* logits, int ldl, const float* row_max,
+                           const float* row_sumexp, const int32_t* row_argmax, const float* q, int ldq,
+                           const int32_t* draft, int V, float temperature, const float* u, int32_t* out_len,
+                           int32_t* out_tokens, void* workspace, size_t workspace_bytes, void* stream) {
+  int st = check_accept(B, row_offsets, logits, ldl, row_max, row_sumexp, row_argmax, q, ldq, draft, V, temperature,
+                        u, out_len, out_tokens);
+  if (st) return st;
+  if (!workspace) return fail(SV_EINVAL, "workspace must be non-null");
+  if (!aligned(workspace, 256)) return fail(SV_EINVAL, "workspace must be 256-byte aligned");
+  const size_t need = accept_bytes(B, row_offsets[B]);
+  if (workspace_bytes < need) return fail(SV_EINVAL, "workspace too small: %zu < %zu", workspace_bytes, need);
+  return accept_internal(B, row_offsets, logits, ldl, row_max, row_sumexp, row_argmax, q, ldq, draft, V,
+                         temperature, u, out_len, out_tokens, workspace, static_cast<cudaStream_t>(stream));
 }
 
 int sv_spec_accept(const float* logits, int ldl, const float* row_max, const float* row_sumexp,

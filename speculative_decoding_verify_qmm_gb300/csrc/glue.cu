@@ -4,6 +4,7 @@
 
 #include "sv_kernels.h"
 #include "sv_ptx.cuh"
+#include "sv_rowops.cuh"
 
 namespace sv {
 
@@ -15,18 +16,7 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const __nv_bfloat16* __res
   const int m = blockIdx.x, tid = threadIdx.x;
   const __nv_bfloat16* row = x + (size_t)m * ldx;
   __shared__ float red[256];
-  float ss = 0.f;
-  for (int k = tid; k < H; k += 256) {
-    const float v = __bfloat162float(row[k]);
-    ss = fmaf(v, v, ss);
-  }
-  red[tid] = ss;
-  __syncthreads();
-  for (int s = 128; s; s >>= 1) {
-    if (tid < s) red[tid] += red[tid + s];
-    __syncthreads();
-  }
-  const float r = 1.f / sqrtf(red[0] / (float)H + eps);
+  const float r = rms_scale_256(row, H, eps, red);
   for (int k = tid; k < H; k += 256) {
     float v = __bfloat162float(row[k]) * r;
     if (w) v *= __bfloat162float(w[k]);

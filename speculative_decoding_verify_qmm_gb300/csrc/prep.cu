@@ -8,6 +8,7 @@
 // The scale is undone once per output row in the epilogue.
 #include "sv_internal.h"
 #include "sv_ptx.cuh"
+#include "sv_rowops.cuh"
 
 namespace sv {
 
@@ -33,19 +34,40 @@ __device__ __forceinline__ int phys_of_slot(int t, int i) {
   return 8 * t + perm;
 }
 
-template <int BITS>
-__global__ void __launch_bounds__(256) prep_kernel(const __nv_bfloat16* __restrict__ x, int ldx, int M, int MP, int K,
-                                                   __half* __restrict__ xp, float* __restrict__ xsum,
-                                                   float* __restrict__ rowscale) {
+// One block per (padded) row.  The row's activation values - x itself, its
+// RMSNorm, or silu(g) * u - are rounded to bf16 exactly as the standalone glue
+// kernels store them, scaled by 2^e and written as fp16 in the order the MMA
+// fragments read them, together with the fp32 sum of each 64-wide group.
+// Values are recomputed from global memory (L2) in each pass so the kernel
+// needs almost no shared memory and fits beside a running matmul CTA.
+template <int MODE>
+__device__ __forceinline__ float prep_value(const PrepArgs& a, const __nv_bfloat16* row, int m, int k, float r) {
+  float v = __bfloat162float(row[k]);
+  if (MODE == PREP_RMSNORM) {
+    v *= r;
+    if (a.w) v *= __bfloat162float(a.w[k]);
+    v = __bfloat162float(__float2bfloat16_rn(v));
+  } else if (MODE == PREP_SWIGLU) {
+    const float u = __bfloat162float(a.x2[(size_t)m * a.ldx2 + k]);
+    v = __bfloat162float(__float2bfloat16_rn(v / (1.f + expf(-v)) * u));
+  }
+  return v;
+}
+
+template <int BITS, int MODE>
+__global__ void __launch_bounds__(256) prep_kernel(PrepArgs a) {
   pdl_trigger();
   pdl_wait();
+  __shared__ float red[256];
   const int m = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const bool live = m < M;
-  const __nv_bfloat16* row = x + (size_t)m * ldx;
-  __shared__ float red[8];
+  const int K = a.K;
+  const bool live = m < a.M;
+  const __nv_bfloat16* row = a.x + (size_t)(live ? m : 0) * a.ldx;
+  float r = 1.f;
+  if (MODE == PREP_RMSNORM && live) r = rms_scale_256(row, K, a.eps, red);
   float mx = 0.f;
   if (live)
-    for (int k = tid; k < K; k += 256) mx = fmaxf(mx, fabsf(__bfloat162float(row[k])));
+    for (int k = tid; k < K; k += 256) mx = fmaxf(mx, fabsf(prep_value<MODE>(a, row, m, k, r)));
   for (int off = 16; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
   if (lane == 0) red[warp] = mx;
   __syncthreads();
@@ -59,19 +81,21 @@ __global__ void __launch_bounds__(256) prep_kernel(const __nv_bfloat16* __restri
     e = e > 100 ? 100 : (e < -100 ? -100 : e);
   }
   const float sc = ldexpf(1.f, e);
-  for (int idx = tid; idx < K; idx += 256) {
-    const int blk = idx >> 5, slot = idx & 31;
-    float v = 0.f;
-    if (live) v = __bfloat162float(row[blk * 32 + phys_of_slot<BITS>(slot >> 3, slot & 7)]) * sc;
-    xp[((size_t)blk * MP + m) * 32 + slot] = __float2half_rn(v);
-  }
+  // warp per group: lane l fills slot l of the group's two 32-element blocks
+  const int phys = phys_of_slot<BITS>(lane >> 3, lane & 7);
   for (int g = warp; g < K / GROUP; g += 8) {
-    float a = 0.f;
-    if (live) a = __bfloat162float(row[g * GROUP + lane]) * sc + __bfloat162float(row[g * GROUP + 32 + lane]) * sc;
-    for (int off = 16; off; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
-    if (lane == 0) xsum[(size_t)g * MP + m] = a;
+    float v0 = 0.f, v1 = 0.f;
+    if (live) {
+      v0 = prep_value<MODE>(a, row, m, g * GROUP + phys, r) * sc;
+      v1 = prep_value<MODE>(a, row, m, g * GROUP + 32 + phys, r) * sc;
+    }
+    a.xp[((size_t)(2 * g) * a.MP + m) * 32 + lane] = __float2half_rn(v0);
+    a.xp[((size_t)(2 * g + 1) * a.MP + m) * 32 + lane] = __float2half_rn(v1);
+    float s = v0 + v1;
+    for (int off = 16; off; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (lane == 0) a.xsum[(size_t)g * a.MP + m] = s;
   }
-  if (tid == 0) rowscale[m] = live ? ldexpf(1.f, -e) : 0.f;
+  if (tid == 0) a.rowscale[m] = live ? ldexpf(1.f, -e) : 0.f;
 }
 
 cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, size_t smem, cudaStream_t s, cudaLaunchAttribute* attr) {
@@ -87,12 +111,22 @@ cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, size_t smem, cudaStream_t s
   return cfg;
 }
 
-cudaError_t launch_prep(const __nv_bfloat16* x, int ldx, int M, int MP, int K, int bits, __half* xp, float* xsum,
-                        float* rowscale, cudaStream_t s) {
+template <int BITS, int MODE>
+static cudaError_t launch_prep_t(const PrepArgs& a, cudaStream_t s) {
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = pdl_config(dim3(MP), dim3(256), 0, s, attr);
-  if (bits == 8) return cudaLaunchKernelEx(&cfg, prep_kernel<8>, x, ldx, M, MP, K, xp, xsum, rowscale);
-  return cudaLaunchKernelEx(&cfg, prep_kernel<4>, x, ldx, M, MP, K, xp, xsum, rowscale);
+  cudaLaunchConfig_t cfg = pdl_config(dim3(a.MP), dim3(256), 0, s, attr);
+  return cudaLaunchKernelEx(&cfg, prep_kernel<BITS, MODE>, a);
+}
+
+cudaError_t launch_prep(const PrepArgs& a, int bits, int mode, cudaStream_t s) {
+  if (bits == 8) {
+    if (mode == PREP_RMSNORM) return launch_prep_t<8, PREP_RMSNORM>(a, s);
+    if (mode == PREP_SWIGLU) return launch_prep_t<8, PREP_SWIGLU>(a, s);
+    return launch_prep_t<8, PREP_PLAIN>(a, s);
+  }
+  if (mode == PREP_RMSNORM) return launch_prep_t<4, PREP_RMSNORM>(a, s);
+  if (mode == PREP_SWIGLU) return launch_prep_t<4, PREP_SWIGLU>(a, s);
+  return launch_prep_t<4, PREP_PLAIN>(a, s);
 }
 
 // One block per row: merge the per-tile (max, argmax, sumexp) triples in tile

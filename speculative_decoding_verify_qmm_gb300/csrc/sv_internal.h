@@ -22,6 +22,17 @@ constexpr int QMM_THREADS = (NCW + 1) * 32;
 constexpr int MAX_M = 32;        // rows per verify block handled by the kernels
 
 enum EpiMode : int { EPI_BF16 = 0, EPI_BF16_RESIDUAL = 1, EPI_LOGITS = 2 };
+enum PrepMode : int { PREP_PLAIN = 0, PREP_RMSNORM = 1, PREP_SWIGLU = 2 };
+constexpr size_t COUNTER_BYTES = 262144;  // zero-between-calls counter prefix of every workspace
+constexpr int MAX_TILES = (int)(COUNTER_BYTES / 4);
+
+struct PrepArgs {
+  const __nv_bfloat16* x; int ldx;      // activations (g for SwiGLU)
+  const __nv_bfloat16* x2; int ldx2;    // u for SwiGLU
+  const __nv_bfloat16* w; float eps;    // RMSNorm weight (nullable) and epsilon
+  int M, MP, K;
+  __half* xp; float* xsum; float* rowscale;
+};
 
 // Stream-K schedule shared by host and device.  Work unit = (tile, k-chunk):
 // units [c*total/grid, (c+1)*total/grid) belong to CTA c.
@@ -47,7 +58,9 @@ struct QmmParams {
   float inv_temp;                  // 1/T, 0 for greedy
 };
 
-// Byte offsets of the pieces of a qmm workspace.
+// Byte offsets of the pieces of a qmm workspace.  The counters always sit in
+// the fixed prefix; the prepared activations depend only on (M, K), so a
+// prepare call and the run calls that consume it agree on where they are.
 struct QmmWorkspace {
   size_t counters, xp, xsum, rowscale, partials, tile_stats, total;
 };
@@ -55,11 +68,32 @@ struct QmmWorkspace {
 Schedule make_schedule(int N, int K, int grid_limit);
 QmmWorkspace qmm_workspace_layout(int M, int N, int K, int grid, bool with_stats);
 int device_sm_count();
+int fail(int status, const char* fmt, ...);
+int check_weight(const uint32_t* wq, const uint16_t* scales, const uint16_t* biases, int N, int K, int bits,
+                 int group, int M);
+int cuda_fail(cudaError_t e, const char* what);
+size_t align256(size_t v);
+bool aligned(const void* p, size_t a);
+size_t prepare_bytes(int M, int K);
+size_t qmm_bytes(int M, int N, int K, bool stats);
+size_t accept_bytes(int B, int rows);
+int qmm_prepare_internal(const uint16_t* x, int ldx, int M, int K, int bits, int mode, const uint16_t* x2, int ldx2,
+                         const uint16_t* w, float eps, void* ws, cudaStream_t s);
+int qmm_run_internal(const uint32_t* wq, const uint16_t* scales, const uint16_t* biases, int N, int K, int bits,
+                     int M, int mode, uint16_t* y, int ldy, const uint16_t* residual, int ldr, float* logits,
+                     int ldl, float temperature, float* row_max, float* row_sumexp, int32_t* row_argmax, void* ws,
+                     cudaStream_t s);
+int check_accept(int B, const int32_t* row_offsets, const float* logits, int ldl, const float* row_max,
+                 const float* row_sumexp, const int32_t* row_argmax, const float* q, int ldq, const int32_t* draft,
+                 int V, float temperature, const float* u, int32_t* out_len, int32_t* out_tokens);
+int accept_internal(int B, const int32_t* offs, const float* logits, int ldl, const float* row_max,
+                    const float* row_sumexp, const int32_t* row_argmax, const float* q, int ldq, const int32_t* draft,
+                    int V, float temperature, const float* u, int32_t* out_len, int32_t* out_tokens, void* ws,
+                    cudaStream_t s);
 cudaError_t read_and_clear_error_word(unsigned int* out);
 
 // Launchers (return cudaError_t of the launch).
-cudaError_t launch_prep(const __nv_bfloat16* x, int ldx, int M, int MP, int K, int bits, __half* xp,
-                        float* xsum, float* rowscale, cudaStream_t s);
+cudaError_t launch_prep(const PrepArgs& a, int bits, int mode, cudaStream_t s);
 cudaError_t launch_qmm(int bits, int NT, const CUtensorMap& tw, const CUtensorMap& ts, const CUtensorMap& tb,
                        const QmmParams& p, cudaStream_t s);
 cudaError_t launch_lmhead_finalize(const float* tile_stats, int tiles_n, int MP, int M, float inv_temp,

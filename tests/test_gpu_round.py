@@ -1,0 +1,167 @@
+"""The fused preparation modes and the whole verify round against the oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import accept as oa, chain, glue, qmm as oq, quant
+import synthetic
+from tests import _model
+from tests._util import assert_close_rms, dev_bf16, host_bf16_bits, host_f32_of_bf16, sub_weight
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("M", [1, 8, 17])
+def test_fused_prepare_is_bit_identical_to_unfused(lib, bits, M):
+    r = synthetic.rng(1200 + M + bits)
+    K, N = 4096, 1024
+    w = _model.to_device(synthetic.quant_weight(r, N, K, bits, synthetic.LARGE_8BIT))
+    h = dev_bf16(synthetic.activations(r, M, K, 5.0))
+    u = dev_bf16(synthetic.activations(r, M, K, 2.0))
+    ws = lib.workspace(lib.qmm_workspace_bytes(M, N, K, bits))
+    # RMSNorm fused vs standalone
+    lib.qmm_prepare(h, K, bits, mode=1, eps=1e-6, workspace=ws)
+    y_fused = lib.qmm_run(w["wq"], w["scales"], w["biases"], K, bits, M, workspace=ws)
+    y_ref = lib.qmm_verify(w["wq"], w["scales"], w["biases"], K, bits, lib.rmsnorm(h))
+    torch.cuda.synchronize()
+    assert torch.equal(y_fused, y_ref)
+    # SwiGLU fused vs standalone
+    lib.qmm_prepare(h, K, bits, mode=2, x2=u, workspace=ws)
+    y_fused = lib.qmm_run(w["wq"], w["scales"], w["biases"], K, bits, M, workspace=ws)
+    y_ref = lib.qmm_verify(w["wq"], w["scales"], w["biases"], K, bits, lib.swiglu(h, u))
+    torch.cuda.synchronize()
+    assert torch.equal(y_fused, y_ref)
+    assert lib.device_error() == 0
+
+
+def _round(lib, model, rows_offsets, h0, T, q=None, draft=None, u=None):
+    M = int(rows_offsets[-1])
+    V = model.vocab
+    hidden = h0.clone()
+    logits = torch.empty((M, V), dtype=torch.float32, device="cuda")
+    out_len = torch.zeros(len(rows_offsets) - 1, dtype=torch.int32, device="cuda")
+    out_tokens = torch.full((M,), -1, dtype=torch.int32, device="cuda")
+    ws = lib.workspace(lib.round_workspace_bytes(model, M))
+    lib.verify_round(model, rows_offsets, hidden, T, logits, out_len, out_tokens, ws, q=q, draft=draft, u=u)
+    torch.cuda.synchronize()
+    return hidden, logits, out_len.cpu().numpy(), out_tokens.cpu().numpy()
+
+
+TINY = dict(hidden=1024, q_dim=1024, kv_dim=512, inter=2048, vocab=1000)
+
+
+@pytest.mark.parametrize("T", [0.0, 1.0])
+def test_tiny_model_round_matches_oracle_chain(lib, T):
+    n_layers, m = 3, 7
+    layers, head = _model.host_model(1300, n_layers, bits=4, stats=synthetic.TINY_4BIT, **TINY)
+    dl = _model.device_layers(layers)
+    dh = _model.to_device(head)
+    r = synthetic.rng(1301)
+    h0 = synthetic.activations(r, m + 1, TINY["hidden"])
+    hs, logits_or, _, am_or, _ = chain.round_logits(h0, layers, head, T)
+    offs = [0, m + 1]
+    for depth in range(1, n_layers + 1):      # per-layer hidden state via prefix models
+        model = lib.make_model(dl[:depth], dh, TINY["hidden"], TINY["q_dim"], TINY["inter"], TINY["vocab"], 4)
+        draft = synthetic.agreeing_drafts(r, am_or[:m], TINY["vocab"])
+        z_q = None
+        q = u = None
+        if T > 0:
+            _, z_q = synthetic.logits_and_draft_probs(r, m, TINY["vocab"])
+            q = torch.from_numpy(z_q).cuda()
+            u = torch.from_numpy(synthetic.accept_uniforms(r, m + 1)).cuda()
+        hidden, logits, n, toks = _round(lib, model, offs, dev_bf16(h0), T, q=q,
+                                         draft=torch.from_numpy(draft).cuda(), u=u)
+        assert_close_rms(host_f32_of_bf16(hidden), quant.bf16_bits_to_f32(hs[depth - 1]),
+                         what="hidden after %d layers" % depth)
+    lg = logits.cpu().numpy()
+    assert_close_rms(lg, logits_or, what="logits")
+    # accept parity on identical (GPU) logits
+    if T > 0:
+        det = oa.sampled_accept_detail(lg, z_q, draft, T, u.cpu().numpy())
+        want = (det["out_len"], det["tokens"])
+    else:
+        want = oa.greedy_accept(lg, draft)
+    assert (int(n[0]), toks[:n[0]].tolist()) == tuple(want)
+    assert lib.device_error() == 0
+
+
+def test_batched_round_four_requests(lib):
+    """Continuous-batching shape: 4 requests x (1 + 7) rows in one round, T = 1."""
+    layers, head = _model.host_model(1400, 2, bits=8, stats=synthetic.LARGE_8BIT, **TINY)
+    model = lib.make_model(_model.device_layers(layers), _model.to_device(head), TINY["hidden"], TINY["q_dim"],
+                           TINY["inter"], TINY["vocab"], 8)
+    r = synthetic.rng(1401)
+    B, m = 4, 7
+    offs = [b * (m + 1) for b in range(B + 1)]
+    h0 = synthetic.activations(r, B * (m + 1), TINY["hidden"])
+    qs = [synthetic.logits_and_draft_probs(r, m, TINY["vocab"])[1] for _ in range(B)]
+    drafts = [synthetic.sample_drafts(r, q) for q in qs]
+    us = [lib.philox_uniforms(99, b, 0, m + 1) for b in range(B)]
+    hidden, logits, n, toks = _round(lib, model, offs, dev_bf16(h0), 1.0,
+                                     q=torch.from_numpy(np.concatenate(qs)).cuda(),
+                                     draft=torch.from_numpy(np.concatenate(drafts)).cuda(), u=torch.cat(us))
+    lg = logits.cpu().numpy()
+    _, logits_or, _, _, _ = chain.round_logits(h0, layers, head, 1.0)
+    assert_close_rms(lg, logits_or, what="batched logits")
+    want = oa.spec_accept_batched(lg, np.concatenate(qs), drafts, offs, 1.0, [x.cpu().numpy() for x in us])
+    for b in range(B):
+        assert (int(n[b]), toks[offs[b]:offs[b] + n[b]].tolist()) == tuple(want[b])
+
+
+QWEN8B = dict(hidden=4096, q_dim=4096, kv_dim=1024, inter=12288, vocab=151936)
+
+
+@pytest.fixture(scope="module")
+def model_8b():
+    layers, head = _model.device_random_model(1500, 36, bits=8, stats=synthetic.LARGE_8BIT, **QWEN8B)
+    yield layers, head
+    del layers, head
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("M,T", [(8, 0.7), (16, 0.0), (1, 0.7)])
+def test_qwen3_8b_round_per_layer_and_head(lib, model_8b, M, T):
+    """Full 36-layer 8-bit round, the benchmark's launch configuration: each checked
+    layer is compared with the oracle applied to the GPU's own input of that layer."""
+    layers, head = model_8b
+    r = synthetic.rng(1600 + M)
+    h0 = dev_bf16(synthetic.activations(r, M, QWEN8B["hidden"]))
+    m = M - 1
+    q = u = None
+    if T > 0 and m:
+        _, qn = synthetic.logits_and_draft_probs(r, m, QWEN8B["vocab"])
+        q = torch.from_numpy(qn).cuda()
+    if T > 0:
+        u = torch.from_numpy(synthetic.accept_uniforms(r, m + 1)).cuda()
+    draft = torch.from_numpy(r.integers(0, QWEN8B["vocab"], m).astype(np.int32)).cuda()
+
+    def run(depth):
+        model = lib.make_model(layers[:depth], head, QWEN8B["hidden"], QWEN8B["q_dim"], QWEN8B["inter"],
+                               QWEN8B["vocab"], 8)
+        return _round(lib, model, [0, M], h0, T, q=q, draft=draft, u=u)
+
+    for depth in (1, 18, 36):
+        before = host_bf16_bits(run(depth - 1)[0]) if depth > 1 else host_bf16_bits(h0)
+        after, logits, n, toks = run(depth)
+        lay = _model.split_device_layer(layers[depth - 1], QWEN8B["q_dim"], QWEN8B["kv_dim"], QWEN8B["inter"])
+        want = chain.layer_forward(before, lay)
+        assert_close_rms(host_f32_of_bf16(after), quant.bf16_bits_to_f32(want), what="layer %d" % depth)
+    # vocab head on sampled rows, from the GPU's final hidden state
+    lg = logits.cpu().numpy()
+    a = glue.rmsnorm(host_bf16_bits(after))
+    rows = np.unique(np.concatenate([r.choice(QWEN8B["vocab"], 2048, replace=False), np.argmax(lg, axis=1)]))
+    hw = _model.host_copy(head)
+    want = oq.qmm_f32(hw["wq"][rows], hw["scales"][rows], hw["biases"][rows], QWEN8B["hidden"], 8, a)
+    assert_close_rms(lg[:, rows], want, what="head rows")
+    # accept on identical logits
+    dn = draft.cpu().numpy()
+    if T > 0:
+        det = oa.sampled_accept_detail(lg, q.cpu().numpy() if q is not None else np.zeros((0, lg.shape[1]), np.float32),
+                                       dn, T, u.cpu().numpy())
+        want_acc = (det["out_len"], det["tokens"])
+    else:
+        want_acc = tuple(oa.greedy_accept(lg, dn))
+    assert (int(n[0]), toks[:n[0]].tolist()) == want_acc
+    assert lib.device_error() == 0
