@@ -84,6 +84,27 @@ int sv_qmm_verify(const uint32_t* wq, const uint16_t* scales, const uint16_t* bi
                   int group, const uint16_t* x, int ldx, int M, uint16_t* y, int ldy, const uint16_t* residual,
                   int ldr, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Allocation-free sv_qmm_verify (no counterpart on the pages: it serves
+ * callers that cannot provide device memory).  Some callers cannot allocate:
+ * a plugin inside a host application that owns all device memory, or a
+ * runtime that forbids cudaMalloc after start-up because it can synchronize
+ * the device.  This form takes no workspace; its scratch lives in one
+ * device array built into the library, sv_qmm_noalloc_scratch_bytes()
+ * bytes (4 MiB) on every GPU that loads the library, held until the process
+ * exits.  Calls whose scratch would exceed it (roughly M = 32 with K above
+ * 20k) return SV_EUNSUPPORTED with the needed size in sv_last_error().
+ * Same arguments and results as sv_qmm_verify, minus the workspace.
+ *   - The first call on a device looks up the array's device address; make
+ *     that first call before any stream capture.
+ *   - Every call shares the array and clears its own counters first; calls
+ *     that overlap on the GPU (other streams, or other host threads) race on
+ *     the array, so order them on one stream.
+ *   - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library call. */
+size_t sv_qmm_noalloc_scratch_bytes(void);
+int sv_qmm_verify_noalloc(const uint32_t* wq, const uint16_t* scales, const uint16_t* biases, int N, int K, int bits,
+                          int group, const uint16_t* x, int ldx, int M, uint16_t* y, int ldy,
+                          const uint16_t* residual, int ldr, void* stream);
+
 /* Split form of sv_qmm_verify for chains of projections.  sv_qmm_prepare
  * converts one activation block into the layout the matmul kernel streams
  * (kept in the workspace); each later sv_qmm_run / sv_lm_head_run with the

@@ -52,6 +52,9 @@ _SIGNATURES = {
     "sv_qmm_workspace_bytes": (_c_size_t, [_c_int, _c_int, _c_int, _c_int]),
     "sv_qmm_verify": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_int, _c_int, _c_int, _c_int, _c_void_p, _c_int,
                                _c_int, _c_void_p, _c_int, _c_void_p, _c_int, _c_void_p, _c_size_t, _c_void_p]),
+    "sv_qmm_noalloc_scratch_bytes": (_c_size_t, []),
+    "sv_qmm_verify_noalloc": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_int, _c_int, _c_int, _c_int, _c_void_p,
+                                       _c_int, _c_int, _c_void_p, _c_int, _c_void_p, _c_int, _c_void_p]),
     "sv_qmm_prepare": (_c_int, [_c_void_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_void_p, _c_int, _c_void_p,
                                 _c_float, _c_void_p, _c_size_t, _c_void_p]),
     "sv_qmm_run": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_void_p,
@@ -158,6 +161,17 @@ class Library:
             _ptr(wq), _ptr(scales), _ptr(biases), N, K, bits, 64, _ptr(x), x.stride(0), M, _ptr(y), y.stride(0),
             _ptr(residual), residual.stride(0) if residual is not None else 0, _ptr(workspace),
             workspace.numel() * workspace.element_size(), _stream(stream)))
+        return y
+
+    def qmm_verify_noalloc(self, wq, scales, biases, K, bits, x, y=None, residual=None, stream=None):
+        """sv_qmm_verify without a workspace (scratch in the library's own device array)."""
+        import torch
+        M, N = x.shape[0], wq.shape[0]
+        if y is None:
+            y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+        self.check(self.lib.sv_qmm_verify_noalloc(
+            _ptr(wq), _ptr(scales), _ptr(biases), N, K, bits, 64, _ptr(x), x.stride(0), M, _ptr(y), y.stride(0),
+            _ptr(residual), residual.stride(0) if residual is not None else 0, _stream(stream)))
         return y
 
     def qmm_prepare(self, x, K, bits, mode=0, x2=None, rms_weight=None, eps=1e-6, workspace=None, stream=None):
