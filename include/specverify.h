@@ -112,10 +112,13 @@ int sv_qmm_verify_noalloc(const uint32_t* wq, const uint16_t* scales, const uint
  * share one preparation.  The preparation can fuse the step that produces
  * the activations:
  *   SV_PREP_PLAIN    x as given (bf16 [M, K], stride ldx)
- *   SV_PREP_RMSNORM  bf16(x / sqrt(mean(x^2) + eps) * weight), weight bf16 [K] or NULL = 1
- *   SV_PREP_SWIGLU   bf16(silu(x) * x2) with x2 bf16 [M, K] (stride ldx2)
- * The fused results are bit-identical to sv_rmsnorm / sv_swiglu followed by
- * SV_PREP_PLAIN.  Workspace: sv_qmm_workspace_bytes() of the run that follows. */
+ *   SV_PREP_RMSNORM  x / sqrt(mean(x^2) + eps) * weight, weight bf16 [K] or NULL = 1;
+ *                    the row scale is applied in fp32 to the matmul output, so
+ *                    the normalized row is never rounded to bf16 (the result
+ *                    differs from sv_rmsnorm + SV_PREP_PLAIN only by that rounding)
+ *   SV_PREP_SWIGLU   bf16(silu(x) * x2) with x2 bf16 [M, K] (stride ldx2); bit-identical
+ *                    to sv_swiglu followed by SV_PREP_PLAIN
+ * Workspace: sv_qmm_workspace_bytes() of the run that follows. */
 enum { SV_PREP_PLAIN = 0, SV_PREP_RMSNORM = 1, SV_PREP_SWIGLU = 2 };
 int sv_qmm_prepare(const uint16_t* x, int ldx, int M, int K, int bits, int mode, const uint16_t* x2, int ldx2,
                    const uint16_t* rms_weight, float eps, void* workspace, size_t workspace_bytes, void* stream);

@@ -106,26 +106,31 @@ __global__ void __launch_bounds__(ACC_THREADS) accept_kernel(const AcceptParams 
   __threadfence();
 
   // ---- last CTA of the request: locate u[m] * Z
+  __shared__ double s_cw[64], s_cp[64];
+  if (tid < NB) {
+    const double* cs = p.chunk_sums + ((size_t)b * NB + tid) * 2;
+    s_cw[tid] = __ldcg(cs);
+    s_cp[tid] = __ldcg(cs + 1);
+  }
+  __syncthreads();
   if (tid == 0) {
-    const double* cs = p.chunk_sums + (size_t)b * NB * 2;
     double zw = 0.0, zp = 0.0;
-    for (int c = 0; c < NB; ++c) { zw += __ldcg(cs + 2 * c); zp += __ldcg(cs + 2 * c + 1); }
+    for (int c = 0; c < NB; ++c) { zw += s_cw[c]; zp += s_cp[c]; }
     const int use_p = resid && !(zw > 0.0);
-    const int sel = use_p ? 1 : 0;
+    const double* sums = use_p ? s_cp : s_cw;
     const double Z = use_p ? zp : zw;
     const double theta = (double)p.u[r0 + m] * Z;
     double pre = 0.0;
     int cstar = -1;
     for (int c = 0; c < NB; ++c) {
-      const double s = __ldcg(cs + 2 * c + sel);
-      if (pre + s > theta) { cstar = c; break; }
-      pre += s;
+      if (pre + sums[c] > theta) { cstar = c; break; }
+      pre += sums[c];
     }
     int flag = use_p;  // bit 0: draw from p; bit 1: take the last positive weight
     if (cstar < 0) {   // rounding left theta at the total: last chunk with positive weight
       flag |= 2;
       for (int c = NB - 1; c >= 0; --c)
-        if (__ldcg(cs + 2 * c + sel) > 0.0) { cstar = c; break; }
+        if (sums[c] > 0.0) { cstar = c; break; }
       if (cstar < 0) cstar = NB - 1;
     }
     s_cstar = cstar;

@@ -74,10 +74,10 @@ QmmWorkspace qmm_workspace_layout(int M, int N, int K, int grid, bool with_stats
   w.counters = 0;     off = COUNTER_BYTES;         // tiles <= MAX_TILES is checked by the callers
   (void)tiles;
   w.xp = off;         off = align256(off + (size_t)K * MP * 2);
-  w.xsum = off;       off = align256(off + (size_t)(K / GROUP) * MP * 4);
-  w.rowscale = off;   off = align256(off + (size_t)MP * 4);
+  w.xsum = off;       off = align256(off + (size_t)(K / KC) * (GPS + 1) * MP * 4);
+  w.rms = off;        off = align256(off + (size_t)(K / KC + 1) * MP * 4);
   w.partials = off;   off = align256(off + (size_t)grid * 2 * BN * MP * 4);
-  w.tile_stats = off; off = align256(off + (with_stats ? (size_t)((N + BN - 1) / BN) * MP * 12 : 0));
+  w.tile_stats = off; off = align256(off + (with_stats ? (size_t)((N + BN - 1) / BN) * 2 * MP * 12 : 0));
   w.total = off;
   return w;
 }
@@ -157,7 +157,7 @@ static int prepare_qmm(QmmCall& c, const uint32_t* wq, const uint16_t* scales, c
   p.counters = reinterpret_cast<int*>(base + L.counters);
   p.xp = reinterpret_cast<const __half*>(base + L.xp);
   p.xsum = reinterpret_cast<const float*>(base + L.xsum);
-  p.rowscale = reinterpret_cast<const float*>(base + L.rowscale);
+  p.rms = reinterpret_cast<const float*>(base + L.rms);
   p.partials = reinterpret_cast<float*>(base + L.partials);
   p.tile_stats = with_stats ? reinterpret_cast<float*>(base + L.tile_stats) : nullptr;
   return SV_OK;
@@ -198,7 +198,8 @@ int qmm_prepare_internal(const uint16_t* x, int ldx, int M, int K, int bits, int
   a.K = K;
   a.xp = reinterpret_cast<__half*>(base + L.xp);
   a.xsum = reinterpret_cast<float*>(base + L.xsum);
-  a.rowscale = reinterpret_cast<float*>(base + L.rowscale);
+  a.rms = reinterpret_cast<float*>(base + L.rms);
+  a.mode = mode;
   cudaError_t e = launch_prep(a, bits, mode, s);
   if (e != cudaSuccess) return cuda_fail(e, "prepare launch");
   return SV_OK;
@@ -223,7 +224,7 @@ int qmm_run_internal(const uint32_t* wq, const uint16_t* scales, const uint16_t*
   cudaError_t e = launch_qmm(bits, c.p.MP / 8, c.tw, c.ts, c.tb, c.p, s);
   if (e != cudaSuccess) return cuda_fail(e, "qmm launch");
   if (stats && (row_max || row_sumexp || row_argmax)) {
-    e = launch_lmhead_finalize(c.p.tile_stats, c.p.sch.tiles_n, c.p.MP, M, c.p.inv_temp, row_max, row_sumexp,
+    e = launch_lmhead_finalize(c.p.tile_stats, c.p.sch.tiles_n * 2, c.p.MP, M, c.p.inv_temp, row_max, row_sumexp,
                                row_argmax, s);
     if (e != cudaSuccess) return cuda_fail(e, "lm_head finalize launch");
   }

@@ -8,7 +8,6 @@
 // The scale is undone once per output row in the epilogue.
 #include "sv_internal.h"
 #include "sv_ptx.cuh"
-#include "sv_rowops.cuh"
 
 namespace sv {
 
@@ -24,54 +23,63 @@ cudaError_t read_and_clear_error_word(unsigned int* out) {
   return e;
 }
 
-// Physical offset (within a 32-element block) of slot i of quad-thread t, matching
-// the order in which the MMA fragments consume codes (see qmm_kernel.cuh).
+// Slot (position in the 32-element block as the MMA fragments read it) of the
+// element at physical offset p within its 32-element block.  The codes are
+// consumed in a permuted k order (see qmm_kernel.cuh); permuting the
+// activations the same way keeps the contraction exact.
 template <int BITS>
-__device__ __forceinline__ int phys_of_slot(int t, int i) {
-  if (BITS == 8) return i < 4 ? 4 * t + i : 16 + 4 * t + (i - 4);
-  // 4-bit: slots pair nibble j with nibble j + 4 of the thread's word
-  const int perm = (i & 1) ? (i >> 1) + 4 : (i >> 1);
-  return 8 * t + perm;
-}
-
-// One block per (padded) row.  The row's activation values - x itself, its
-// RMSNorm, or silu(g) * u - are rounded to bf16 exactly as the standalone glue
-// kernels store them, scaled by 2^e and written as fp16 in the order the MMA
-// fragments read them, together with the fp32 sum of each 64-wide group.
-// Values are recomputed from global memory (L2) in each pass so the kernel
-// needs almost no shared memory and fits beside a running matmul CTA.
-template <int MODE>
-__device__ __forceinline__ float prep_value(const PrepArgs& a, const __nv_bfloat16* row, int m, int k, float r) {
-  float v = __bfloat162float(row[k]);
-  if (MODE == PREP_RMSNORM) {
-    v *= r;
-    if (a.w) v *= __bfloat162float(a.w[k]);
-    v = __bfloat162float(__float2bfloat16_rn(v));
-  } else if (MODE == PREP_SWIGLU) {
-    const float u = __bfloat162float(a.x2[(size_t)m * a.ldx2 + k]);
-    v = __bfloat162float(__float2bfloat16_rn(v / (1.f + expf(-v)) * u));
+__device__ __forceinline__ int slot_of_phys(int p) {
+  if (BITS == 8) {
+    // slot 8t + i holds element 4t + i (i < 4) or 16 + 4t + (i - 4)
+    const int hi = p >> 4, q = p & 15;
+    return 8 * (q >> 2) + 4 * hi + (q & 3);
   }
-  return v;
+  // 4-bit: slot 8t + i holds nibble j = (0, 4, 1, 5, 2, 6, 3, 7)[i] of element block 8t
+  const int j = p & 7;
+  return (p & ~7) + (j < 4 ? 2 * j : 2 * (j - 4) + 1);
 }
 
+// One block per (512-wide k chunk, padded row).  Every step is local to the
+// chunk, so the grid covers the whole activation block at once:
+//   v   = x, bf16(silu(x) * x2) for SwiGLU, or bf16(x * weight) for RMSNorm
+//         (whose row scale 1/sqrt(mean(x^2) + eps) is applied to the matmul
+//         output; this block stores its chunk's sum of x^2 for that),
+//   e   = 15 - exponent of the chunk's max |v|, so v * 2^e lies below 2^15 and
+//         every bf16 value keeps all its significant bits in fp16,
+//   out = fp16(v * 2^e) in MMA order, the fp32 sum of each 64-wide group of
+//         v * 2^e, and 2^-e.
 template <int BITS, int MODE>
 __global__ void __launch_bounds__(256) prep_kernel(PrepArgs a) {
   pdl_trigger();
   pdl_wait();
-  __shared__ float red[256];
-  const int m = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int K = a.K;
+  __shared__ float red[8];
+  const int c = blockIdx.x, m = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool live = m < a.M;
-  const __nv_bfloat16* row = a.x + (size_t)(live ? m : 0) * a.ldx;
-  float r = 1.f;
-  if (MODE == PREP_RMSNORM && live) r = rms_scale_256(row, K, a.eps, red);
-  float mx = 0.f;
-  if (live)
-    for (int k = tid; k < K; k += 256) mx = fmaxf(mx, fabsf(prep_value<MODE>(a, row, m, k, r)));
+  const int k0 = c * KC + 2 * tid;  // this thread's two elements
+  float v[2] = {0.f, 0.f}, sq = 0.f;
+  if (live) {
+    const __nv_bfloat16* row = a.x + (size_t)m * a.ldx;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      float x = __bfloat162float(row[k0 + i]);
+      if (MODE == PREP_RMSNORM) {
+        sq = fmaf(x, x, sq);
+        if (a.w) x = __bfloat162float(__float2bfloat16_rn(x * __bfloat162float(a.w[k0 + i])));
+      } else if (MODE == PREP_SWIGLU) {
+        const float u = __bfloat162float(a.x2[(size_t)m * a.ldx2 + k0 + i]);
+        x = __bfloat162float(__float2bfloat16_rn(x / (1.f + expf(-x)) * u));
+      }
+      v[i] = x;
+    }
+  }
+  float mx = fmaxf(fabsf(v[0]), fabsf(v[1]));
   for (int off = 16; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  if (MODE == PREP_RMSNORM)
+    for (int off = 16; off; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
   if (lane == 0) red[warp] = mx;
   __syncthreads();
   mx = red[0];
+#pragma unroll
   for (int w = 1; w < 8; ++w) mx = fmaxf(mx, red[w]);
   int e = 0;
   if (mx > 0.f && mx <= 3.0e38f) {
@@ -81,21 +89,30 @@ __global__ void __launch_bounds__(256) prep_kernel(PrepArgs a) {
     e = e > 100 ? 100 : (e < -100 ? -100 : e);
   }
   const float sc = ldexpf(1.f, e);
-  // warp per group: lane l fills slot l of the group's two 32-element blocks
-  const int phys = phys_of_slot<BITS>(lane >> 3, lane & 7);
-  for (int g = warp; g < K / GROUP; g += 8) {
-    float v0 = 0.f, v1 = 0.f;
-    if (live) {
-      v0 = prep_value<MODE>(a, row, m, g * GROUP + phys, r) * sc;
-      v1 = prep_value<MODE>(a, row, m, g * GROUP + 32 + phys, r) * sc;
-    }
-    a.xp[((size_t)(2 * g) * a.MP + m) * 32 + lane] = __float2half_rn(v0);
-    a.xp[((size_t)(2 * g + 1) * a.MP + m) * 32 + lane] = __float2half_rn(v1);
-    float s = v0 + v1;
-    for (int off = 16; off; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    if (lane == 0) a.xsum[(size_t)g * a.MP + m] = s;
+  float gs = 0.f;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int k = 2 * tid + i;  // offset within the chunk
+    const float y = v[i] * sc;
+    gs += y;
+    a.xp[((size_t)(c * (KC / 32) + (k >> 5)) * a.MP + m) * 32 + slot_of_phys<BITS>(k & 31)] = __float2half_rn(y);
   }
-  if (tid == 0) a.rowscale[m] = live ? ldexpf(1.f, -e) : 0.f;
+  // warp w covers elements 64w .. 64w+63 of the chunk: exactly group w
+  for (int off = 16; off; off >>= 1) gs += __shfl_xor_sync(0xffffffffu, gs, off);
+  float* xs = a.xsum + (size_t)c * (GPS + 1) * a.MP;
+  if (lane == 0) xs[warp * a.MP + m] = gs;
+  if (tid == 0) xs[GPS * a.MP + m] = live ? ldexpf(1.f, -e) : 0.f;
+  if (MODE == PREP_RMSNORM) {
+    __syncthreads();
+    if (lane == 0) red[warp] = sq;
+    __syncthreads();
+    if (tid == 0) {
+      float t = 0.f;
+      for (int w = 0; w < 8; ++w) t += red[w];
+      a.rms[(size_t)c * a.MP + m] = t;
+    }
+  }
+  if (c == 0 && tid == 0) a.rms[(size_t)(a.K / KC) * a.MP + m] = MODE == PREP_RMSNORM ? a.eps : -1.f;
 }
 
 cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, size_t smem, cudaStream_t s, cudaLaunchAttribute* attr) {
@@ -114,7 +131,7 @@ cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, size_t smem, cudaStream_t s
 template <int BITS, int MODE>
 static cudaError_t launch_prep_t(const PrepArgs& a, cudaStream_t s) {
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = pdl_config(dim3(a.MP), dim3(256), 0, s, attr);
+  cudaLaunchConfig_t cfg = pdl_config(dim3(a.K / KC, a.MP), dim3(256), 0, s, attr);
   return cudaLaunchKernelEx(&cfg, prep_kernel<BITS, MODE>, a);
 }
 
@@ -129,9 +146,10 @@ cudaError_t launch_prep(const PrepArgs& a, int bits, int mode, cudaStream_t s) {
   return launch_prep_t<4, PREP_PLAIN>(a, s);
 }
 
-// One block per row: merge the per-tile (max, argmax, sumexp) triples in tile
-// order.  Ties keep the lowest vocabulary index; sum-exp is rescaled to the
-// global maximum and added in fp64 in a fixed tree order.
+// One block per row: merge the per-slice (max, argmax, sumexp) triples of the
+// 32-column slices in order.  Ties keep the lowest vocabulary index; each
+// slice's sum-exp is rescaled to the global maximum (fp32 exp of a
+// non-positive argument) and the terms are added in fp64 in a fixed order.
 __global__ void __launch_bounds__(256) lmhead_finalize_kernel(const float* __restrict__ ts, int tiles, int MP,
                                                               float inv_temp, float* row_max, float* row_sumexp,
                                                               int32_t* row_argmax) {
@@ -166,7 +184,7 @@ __global__ void __launch_bounds__(256) lmhead_finalize_kernel(const float* __res
     for (int t = tid; t < tiles; t += 256) {
       const float v = ts[((size_t)t * MP + m) * 3];
       const float se = ts[((size_t)t * MP + m) * 3 + 2];
-      acc += (double)se * exp(((double)v - (double)best) * (double)inv_temp);
+      acc += (double)(se * expf((v - best) * inv_temp));
     }
     sd[tid] = acc;
     __syncthreads();

@@ -8,7 +8,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
-#include "../../include/specverify.h"
+#include "specverify.h"
 
 namespace sv {
 
@@ -17,21 +17,23 @@ constexpr int GROUP = 64;        // weights per quantization group (along K)
 constexpr int BN = 64;           // weight rows per CTA tile
 constexpr int KC = 512;          // k per pipeline stage (8 groups)
 constexpr int GPS = KC / GROUP;  // groups per stage
-constexpr int NCW = 4;           // consumer warps per CTA (each owns 2 groups of a stage)
+constexpr int NCW = 8;           // consumer warps per CTA: 2 row halves x 4 k-quarters
 constexpr int QMM_THREADS = (NCW + 1) * 32;
 constexpr int MAX_M = 32;        // rows per verify block handled by the kernels
 
 enum EpiMode : int { EPI_BF16 = 0, EPI_BF16_RESIDUAL = 1, EPI_LOGITS = 2 };
 enum PrepMode : int { PREP_PLAIN = 0, PREP_RMSNORM = 1, PREP_SWIGLU = 2 };
 constexpr size_t COUNTER_BYTES = 262144;  // zero-between-calls counter prefix of every workspace
-constexpr int MAX_TILES = (int)(COUNTER_BYTES / 4);
+constexpr int MAX_TILES = (int)(COUNTER_BYTES / 8);  // two counters (row halves) per tile
 
 struct PrepArgs {
   const __nv_bfloat16* x; int ldx;      // activations (g for SwiGLU)
   const __nv_bfloat16* x2; int ldx2;    // u for SwiGLU
   const __nv_bfloat16* w; float eps;    // RMSNorm weight (nullable) and epsilon
-  int M, MP, K;
-  __half* xp; float* xsum; float* rowscale;
+  int M, MP, K, mode;
+  __half* xp;                           // [K/32][MP][32] fp16 (scaled, MMA order)
+  float* xsum;                          // [K/512][9][MP]: 8 group sums, then 2^-e of the chunk
+  float* rms;                           // [K/512 + 1][MP]: chunk sums of x^2, then eps (or -1: no RMSNorm)
 };
 
 // Stream-K schedule shared by host and device.  Work unit = (tile, k-chunk):
@@ -44,17 +46,17 @@ struct QmmParams {
   Schedule sch;
   int M, MP;                       // rows, rows padded to the n8 MMA tile
   // prepared activations (written by the prep kernel into the workspace)
-  const __half* xp;                // [K/32][MP][32] fp16, scaled by 2^e[m], permuted
-  const float* xsum;               // [K/64][MP] fp32, group sums of the scaled rows
-  const float* rowscale;           // [MP] 2^-e[m]
-  float* partials;                 // [grid][2][BN*MP]
-  int* counters;                   // [tiles_n], zero between calls
+  const __half* xp;                // [K/32][MP][32] fp16, scaled by 2^e per (row, chunk), permuted
+  const float* xsum;               // [K/512][9][MP]: group sums of the scaled rows, then 2^-e
+  const float* rms;                // [K/512 + 1][MP]: RMSNorm partials and eps (eps < 0: none)
+  float* partials;                 // [grid][2 slots][2 halves][32*MP]
+  int* counters;                   // [tiles_n][2], zero between calls
   // epilogue
   int mode;
   __nv_bfloat16* y; int ldy;       // EPI_BF16 / EPI_BF16_RESIDUAL
   const __nv_bfloat16* res; int ldres;
   float* logits; int ldl;          // EPI_LOGITS
-  float* tile_stats;               // [tiles_n][MP][3] (max, argmax bits, sumexp)
+  float* tile_stats;               // [tiles_n*2][MP][3] per 32-row half (max, argmax bits, sumexp)
   float inv_temp;                  // 1/T, 0 for greedy
 };
 
@@ -62,7 +64,7 @@ struct QmmParams {
 // the fixed prefix; the prepared activations depend only on (M, K), so a
 // prepare call and the run calls that consume it agree on where they are.
 struct QmmWorkspace {
-  size_t counters, xp, xsum, rowscale, partials, tile_stats, total;
+  size_t counters, xp, xsum, rms, partials, tile_stats, total;
 };
 
 Schedule make_schedule(int N, int K, int grid_limit);

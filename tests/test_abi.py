@@ -84,3 +84,14 @@ def test_glue_and_philox_argument_errors_on_host(raw):
     assert raw.sv_rmsnorm(P(16), 32, 2, 64, None, 1e-6, P(16), 64, None) == binding.SV_EINVAL
     assert raw.sv_residual_add(None, 64, P(16), 64, 2, 64, None) == binding.SV_EINVAL
     assert raw.sv_swiglu(P(16), 64, P(16), 64, 2, 64, P(16), 10, None) == binding.SV_EINVAL
+
+
+def test_bf16_ulp_helper():
+    import numpy as np
+    from oracle import quant
+    from tests._util import bf16_ulp
+    x = np.array([1.0, 1.5, 2.0, 3.0, 0.75, -6.0, 1e-3], dtype=np.float32)
+    # the next bf16 value above |x| is |x| + ulp for every x exactly representable in bf16
+    bits = quant.f32_to_bf16_bits(np.abs(x))
+    nxt = quant.bf16_bits_to_f32((bits + 1).astype(np.uint16)).astype(np.float64)
+    assert np.allclose(nxt - quant.bf16_bits_to_f32(bits), bf16_ulp(x), rtol=0, atol=0)

@@ -6,7 +6,7 @@ import torch
 
 from oracle import qmm as oq
 import synthetic
-from tests._util import assert_close_rms, dev_bf16, dev_weight, host_f32_of_bf16, host_bf16_bits, sub_weight
+from tests._util import assert_close_bf16, assert_close_rms, dev_bf16, dev_weight, host_f32_of_bf16, host_bf16_bits, sub_weight
 from oracle import quant
 
 pytestmark = pytest.mark.gpu
@@ -31,7 +31,7 @@ def test_tiny_4bit_layer(lib, M):
     w = synthetic.quant_weight(r, 1024, 1024, 4, synthetic.TINY_4BIT)
     x = synthetic.activations(r, M, 1024)
     y = _run(lib, w, x)
-    assert_close_rms(host_f32_of_bf16(y), _oracle_f32(w, x), what="tiny M=%d" % M)
+    assert_close_bf16(host_f32_of_bf16(y), _oracle_f32(w, x), what="tiny M=%d" % M)
     assert lib.device_error() == 0
 
 
@@ -43,7 +43,7 @@ def test_ragged_shapes(lib, bits, N, K, M):
     w = synthetic.quant_weight(r, N, K, bits, synthetic.LARGE_8BIT if bits == 8 else synthetic.TINY_4BIT)
     x = synthetic.activations(r, M, K)
     y = _run(lib, w, x)
-    assert_close_rms(host_f32_of_bf16(y), _oracle_f32(w, x), what="N=%d K=%d M=%d" % (N, K, M))
+    assert_close_bf16(host_f32_of_bf16(y), _oracle_f32(w, x), what="N=%d K=%d M=%d" % (N, K, M))
 
 
 SHAPES_8B = {"q": (4096, 4096), "k": (1024, 4096), "o": (4096, 4096), "gate": (12288, 4096), "down": (4096, 12288)}
@@ -59,7 +59,7 @@ def test_qwen3_8b_projection_shapes(lib, name):
     want = _oracle_f32(w, x17)
     for M in (1, 2, 4, 6, 8, 12, 16, 17):
         y = _run(lib, w, x17[:M])
-        assert_close_rms(host_f32_of_bf16(y), want[:M], what="%s M=%d" % (name, M))
+        assert_close_bf16(host_f32_of_bf16(y), want[:M], what="%s M=%d" % (name, M))
 
 
 def test_residual_in_place_and_strides(lib):
@@ -78,7 +78,7 @@ def test_residual_in_place_and_strides(lib):
     t = oq.qmm_verify(w["wq"], w["scales"], w["biases"], K, 8, x)
     from oracle import glue
     want = quant.bf16_bits_to_f32(glue.residual_add(h, t))
-    assert_close_rms(host_f32_of_bf16(hd), want, what="residual")
+    assert_close_bf16(host_f32_of_bf16(hd), want, what="residual")
 
 
 def test_bitwise_reproducible(lib):
@@ -101,7 +101,7 @@ def test_large_activation_range(lib):
     y = host_f32_of_bf16(_run(lib, w, xb))
     want = _oracle_f32(w, xb)
     for m in range(5):
-        assert_close_rms(y[m:m + 1], want[m:m + 1], what="row %d" % m)
+        assert_close_bf16(y[m:m + 1], want[m:m + 1], what="row %d" % m)
 
 
 def test_host_rejections(lib):
