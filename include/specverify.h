@@ -220,13 +220,19 @@ int sv_swiglu(const uint16_t* g, int ldg, const uint16_t* u, int ldu, int M, int
  * sv_qweight: one quantized matrix [N, K] in the format above (device pointers).
  * sv_layer:   qkv  = q | k | v stacked along N (first q_dim rows are q), K = hidden
  *             o    = [hidden, q_dim]
- *             gate_up = gate | up stacked along N (inter rows each), K = hidden
+ *             gate_up = [2*inter, hidden], gate and up rows interleaved in blocks
+ *                    of 64: rows 128j .. 128j+63 are gate rows 64j .. 64j+63 and
+ *                    rows 128j+64 .. 128j+127 the matching up rows
  *             down = [hidden, inter]
+ *             hidden, q_dim and inter must be multiples of 512.
  * sv_model:   `layers` is a HOST array of n_layers entries; every layer's qkv
  *             has the same N; lm_head = [vocab, hidden].
  *
- * sv_verify_round enqueues the whole round (8 launches per layer plus 4) on
- * `stream`; it can be captured into a CUDA graph.  Arguments:
+ * sv_verify_round enqueues the whole round on `stream` as four launches
+ * (input preparation, all 4 * n_layers + 1 projections in one persistent
+ * cooperative kernel, the row-statistics merge, the accept step); it can be
+ * captured into a CUDA graph.  At most 67 layers.  Arguments:
+ *   plan    the model's round plan (device, from sv_round_plan_init below).
  *   B, row_offsets (HOST int32 [B+1]): requests stacked into M = row_offsets[B]
  *     rows, 1 <= M <= 32, each as in sv_spec_accept_batched.
  *   hidden  bf16 [M, hidden] (stride ldh): the rows' input hidden states;
@@ -235,6 +241,10 @@ int sv_swiglu(const uint16_t* g, int ldg, const uint16_t* u, int ldu, int M, int
  *     sv_spec_accept_batched.
  *   logits  fp32 [M, vocab] (stride ldl): the round's target logits.
  *   out_len int32 [B], out_tokens int32 [M]: the accept result.
+ *   event_start, event_stop: optional cudaEvent_t (NULL to skip) recorded on
+ *     `stream` just before and after the launch that runs all the projections,
+ *     for timing it (recording them adds a dependency that delays that launch
+ *     by the previous launch's drain).
  * Workspace: sv_round_workspace_bytes(model, M) bytes (zero prefix rule above). */
 typedef struct {
   const uint32_t* wq;
@@ -253,10 +263,23 @@ typedef struct {
 } sv_model;
 
 size_t sv_round_workspace_bytes(const sv_model* model, int rows);
-int sv_verify_round(const sv_model* model, int B, const int32_t* row_offsets, uint16_t* hidden, int ldh,
+
+/* Round plan: the TMA descriptors of every projection of `model`, built once
+ * per model in caller-owned device memory of sv_round_plan_bytes(model) bytes
+ * (256-byte aligned).  sv_round_plan_init checks the model (as
+ * sv_verify_round does), encodes the descriptors and copies them to `plan`
+ * synchronously, so it must not be called while a stream is being captured.
+ * The library remembers the weight pointers and shapes each plan was built
+ * for; sv_verify_round refuses (SV_EINVAL) a plan built for another model.
+ * Rebuild the plan whenever a weight pointer changes.  sv_round_plan_bytes
+ * returns 0 for a null model or more than 67 layers. */
+size_t sv_round_plan_bytes(const sv_model* model);
+int sv_round_plan_init(const sv_model* model, void* plan, size_t plan_bytes);
+
+int sv_verify_round(const sv_model* model, const void* plan, int B, const int32_t* row_offsets, uint16_t* hidden, int ldh,
                     float temperature, const float* q, int ldq, const int32_t* draft, const float* u, float* logits,
                     int ldl, int32_t* out_len, int32_t* out_tokens, void* workspace, size_t workspace_bytes,
-                    void* stream);
+                    void* stream, void* event_start, void* event_stop);
 
 #ifdef __cplusplus
 }

@@ -64,9 +64,11 @@ _SIGNATURES = {
                                 _c_void_p, _c_int, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_size_t,
                                 _c_void_p]),
     "sv_round_workspace_bytes": (_c_size_t, [_c_model_p, _c_int]),
-    "sv_verify_round": (_c_int, [_c_model_p, _c_int, _c_i32_p, _c_void_p, _c_int, _c_float, _c_void_p, _c_int,
+    "sv_round_plan_bytes": (_c_size_t, [_c_model_p]),
+    "sv_round_plan_init": (_c_int, [_c_model_p, _c_void_p, _c_size_t]),
+    "sv_verify_round": (_c_int, [_c_model_p, _c_void_p, _c_int, _c_i32_p, _c_void_p, _c_int, _c_float, _c_void_p, _c_int,
                                  _c_void_p, _c_void_p, _c_void_p, _c_int, _c_void_p, _c_void_p, _c_void_p,
-                                 _c_size_t, _c_void_p]),
+                                 _c_size_t, _c_void_p, _c_void_p, _c_void_p]),
     "sv_lm_head_verify": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_int, _c_int, _c_int, _c_int, _c_void_p,
                                    _c_int, _c_int, _c_float, _c_void_p, _c_int, _c_void_p, _c_void_p, _c_void_p,
                                    _c_void_p, _c_size_t, _c_void_p]),
@@ -229,9 +231,9 @@ class Library:
         return logits
 
     # ---------------------------------------------------------------- round
-    @staticmethod
-    def make_model(layers, lm_head, hidden, q_dim, inter, vocab, bits, rms_eps=1e-6):
-        """A ctypes sv_model over device weight dicts {'wq','scales','biases'} (kept alive by the caller).
+    def make_model(self, layers, lm_head, hidden, q_dim, inter, vocab, bits, rms_eps=1e-6):
+        """A ctypes sv_model over device weight dicts {'wq','scales','biases'}, with its round plan
+        (``model.plan``, a device tensor built by sv_round_plan_init).
 
         ``layers``: list of dicts with keys qkv, o, gate_up, down."""
         def qw(w):
@@ -242,20 +244,29 @@ class Library:
         m = Model(len(layers), hidden, q_dim, inter, vocab, bits, rms_eps, arr, qw(lm_head))
         # the struct holds raw device pointers: keep the tensors (and the array) alive with it
         m._keep = (arr, layers, lm_head)
+        nbytes = self.lib.sv_round_plan_bytes(ctypes.byref(m))
+        if nbytes == 0:
+            raise SVError(SV_EINVAL, "sv_round_plan_bytes: model rejected")
+        m.plan = self.workspace(nbytes, device=lm_head["wq"].device)
+        self.check(self.lib.sv_round_plan_init(ctypes.byref(m), _ptr(m.plan), nbytes))
         return m
 
     def round_workspace_bytes(self, model, rows):
         return self.lib.sv_round_workspace_bytes(ctypes.byref(model), rows)
 
     def verify_round(self, model, row_offsets, hidden, temperature, logits, out_len, out_tokens, workspace,
-                     q=None, draft=None, u=None, stream=None):
+                     q=None, draft=None, u=None, stream=None, events=None):
+        """events: optional (start, stop) torch.cuda.Event pair recorded around the matmul launch."""
         B = len(row_offsets) - 1
         offs = (ctypes.c_int32 * (B + 1))(*[int(v) for v in row_offsets])
+        ev0 = ev1 = None
+        if events is not None:
+            ev0, ev1 = (ctypes.c_void_p(e.cuda_event) for e in events)
         self.check(self.lib.sv_verify_round(
-            ctypes.byref(model), B, offs, _ptr(hidden), hidden.stride(0), float(temperature), _ptr(q),
+            ctypes.byref(model), _ptr(model.plan), B, offs, _ptr(hidden), hidden.stride(0), float(temperature), _ptr(q),
             q.stride(0) if q is not None else 0, _ptr(draft), _ptr(u), _ptr(logits), logits.stride(0),
             _ptr(out_len), _ptr(out_tokens), _ptr(workspace), workspace.numel() * workspace.element_size(),
-            _stream(stream)))
+            _stream(stream), ev0, ev1))
 
     # --------------------------------------------------------------- accept
     def accept_workspace_bytes(self, B, rows):

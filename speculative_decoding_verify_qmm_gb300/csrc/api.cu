@@ -2,11 +2,11 @@
 // tensor-map encoding and kernel dispatch.  Nothing here allocates device
 // memory and nothing throws across the boundary.
 #include <cudaTypedefs.h>
-
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <cstddef>
 #include <mutex>
 
 #include "sv_internal.h"
@@ -15,14 +15,24 @@
 
 namespace sv {
 
-cudaError_t launch_qmm_b4(int NT, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const QmmParams&,
-                          cudaStream_t);
-cudaError_t launch_qmm_b8(int NT, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const QmmParams&,
-                          cudaStream_t);
+cudaError_t launch_stream_b4(const StreamParams& p, cudaStream_t s);
+cudaError_t launch_stream_b8(const StreamParams& p, cudaStream_t s);
+int stream_max_grid_b4(int MP);
+int stream_max_grid_b8(int MP);
 
-cudaError_t launch_qmm(int bits, int NT, const CUtensorMap& tw, const CUtensorMap& ts, const CUtensorMap& tb,
-                       const QmmParams& p, cudaStream_t s) {
-  return bits == 8 ? launch_qmm_b8(NT, tw, ts, tb, p, s) : launch_qmm_b4(NT, tw, ts, tb, p, s);
+cudaError_t launch_stream(int bits, const StreamParams& p, cudaStream_t s) {
+  return bits == 8 ? launch_stream_b8(p, s) : launch_stream_b4(p, s);
+}
+
+int stream_max_grid(int bits, int MP) {
+  static std::mutex mu;
+  static int cache[64][2][5] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  int& c = cache[dev][bits == 8][MP / 8];
+  if (!c) c = bits == 8 ? stream_max_grid_b8(MP) : stream_max_grid_b4(MP);
+  return c;
 }
 
 static thread_local char g_last[512] = "";
@@ -34,9 +44,7 @@ int fail(int status, const char* fmt, ...) {
   va_end(ap);
   return status;
 }
-int cuda_fail(cudaError_t e, const char* what) {
-  return fail(SV_ECUDA, "%s: %s", what, cudaGetErrorString(e));
-}
+int cuda_fail(cudaError_t e, const char* what) { return fail(SV_ECUDA, "%s: %s", what, cudaGetErrorString(e)); }
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -55,31 +63,47 @@ int device_sm_count() {
   return cache[dev];
 }
 
-Schedule make_schedule(int N, int K, int grid_limit) {
-  Schedule s;
-  s.N = N;
-  s.K = K;
-  s.tiles_n = (N + BN - 1) / BN;
-  s.units_per_tile = K / KC;
-  s.total_units = s.tiles_n * s.units_per_tile;
-  s.grid = s.total_units < grid_limit ? s.total_units : grid_limit;
-  return s;
+Layout workspace_layout(int M, int K_cap, int grid, int stat_tiles, int n_act) {
+  const int MP = 8 * ((M + 7) / 8);
+  const size_t G = (size_t)K_cap / GROUP;
+  Layout L = {};
+  size_t off = COUNTER_BYTES;
+  for (int a = 0; a < n_act; ++a) {
+    L.act[a][0] = off; off = align256(off + (size_t)K_cap * MP * 2);
+    L.act[a][1] = off; off = align256(off + G * 2 * MP * 4);
+    L.act[a][2] = off; off = align256(off + (G + 1) * MP * 4);
+  }
+  L.partials = off;   off = align256(off + (size_t)grid * 2 * BN * MP * 4);
+  L.tile_stats = off; off = align256(off + (size_t)stat_tiles * MP * 12);
+  L.total = off;
+  return L;
 }
 
-QmmWorkspace qmm_workspace_layout(int M, int N, int K, int grid, bool with_stats) {
-  const int MP = 8 * ((M + 7) / 8);
-  const size_t tiles = (size_t)((N + BN - 1) / BN);
-  QmmWorkspace w;
-  size_t off = 0;
-  w.counters = 0;     off = COUNTER_BYTES;         // tiles <= MAX_TILES is checked by the callers
-  (void)tiles;
-  w.xp = off;         off = align256(off + (size_t)K * MP * 2);
-  w.xsum = off;       off = align256(off + (size_t)(K / KC) * (GPS + 1) * MP * 4);
-  w.rms = off;        off = align256(off + (size_t)(K / KC + 1) * MP * 4);
-  w.partials = off;   off = align256(off + (size_t)grid * 2 * BN * MP * 4);
-  w.tile_stats = off; off = align256(off + (with_stats ? (size_t)((N + BN - 1) / BN) * 2 * MP * 12 : 0));
-  w.total = off;
-  return w;
+ActBuf act_buf(void* ws, const Layout& L, int a) {
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  ActBuf b;
+  b.xp = reinterpret_cast<__half*>(base + L.act[a][0]);
+  b.xs = reinterpret_cast<float*>(base + L.act[a][1]);
+  b.sq = reinterpret_cast<float*>(base + L.act[a][2]);
+  return b;
+}
+
+void stream_params_init(StreamParams& p, void* ws, const Layout& L, int M, int grid, float rms_eps) {
+  memset(static_cast<void*>(&p), 0, offsetof(StreamParams, ph));
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  p.M = M;
+  p.MP = 8 * ((M + 7) / 8);
+  p.grid = grid;
+  p.rms_eps = rms_eps;
+  p.act[0] = act_buf(ws, L, 0);
+  p.act[1] = L.act[1][0] ? act_buf(ws, L, 1) : p.act[0];
+  p.partials = reinterpret_cast<float*>(base + L.partials);
+  p.tile_counters = reinterpret_cast<int*>(base + TILE_CTR_OFF);
+  p.pair_counters = reinterpret_cast<int*>(base + PAIR_CTR_OFF);
+  p.grid_bar = reinterpret_cast<unsigned*>(base + GRID_BAR_OFF);
+  p.exit_counter = reinterpret_cast<int*>(base + EXIT_CTR_OFF);
+  p.abort_all = reinterpret_cast<int*>(base + ABORT_OFF);
+  p.tile_stats = reinterpret_cast<float*>(base + L.tile_stats);
 }
 
 // ------------------------------------------------------------- tensor maps
@@ -111,9 +135,22 @@ static int encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base,
   return SV_OK;
 }
 
+int encode_weight_maps(CUtensorMap (&out)[3], const void* wq, const void* scales, const void* biases, int N, int K,
+                       int bits) {
+  const uint64_t row_bytes = (uint64_t)K * bits / 8, G = (uint64_t)(K / GROUP);
+  int st = encode_2d(&out[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, row_bytes, (uint64_t)N, row_bytes, 128, BN,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+  if (st) return st;
+  st = encode_2d(&out[1], CU_TENSOR_MAP_DATA_TYPE_UINT16, scales, G, (uint64_t)N, G * 2, GPS, BN,
+                 CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (st) return st;
+  return encode_2d(&out[2], CU_TENSOR_MAP_DATA_TYPE_UINT16, biases, G, (uint64_t)N, G * 2, GPS, BN,
+                   CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
 // Shared validation of a quantized weight + activation block.
 int check_weight(const uint32_t* wq, const uint16_t* scales, const uint16_t* biases, int N, int K, int bits,
-                        int group, int M) {
+                 int group, int M) {
   if (!wq || !scales || !biases) return fail(SV_EINVAL, "weight pointers must be non-null");
   if (bits != 4 && bits != 8) return fail(SV_EUNSUPPORTED, "bits must be 4 or 8 (got %d)", bits);
   if (group != GROUP) return fail(SV_EUNSUPPORTED, "group size must be 64 (got %d)", group);
@@ -125,41 +162,6 @@ int check_weight(const uint32_t* wq, const uint16_t* scales, const uint16_t* bia
   if (M > MAX_M) return fail(SV_EUNSUPPORTED, "M must be <= 32 (got %d)", M);
   if (!aligned(wq, 16) || !aligned(scales, 16) || !aligned(biases, 16))
     return fail(SV_EINVAL, "wq, scales and biases must be 16-byte aligned");
-  return SV_OK;
-}
-
-struct QmmCall {
-  CUtensorMap tw, ts, tb;
-  QmmParams p;
-};
-
-static int prepare_qmm(QmmCall& c, const uint32_t* wq, const uint16_t* scales, const uint16_t* biases, int N, int K,
-                       int bits, int M, void* ws, bool with_stats) {
-  const int sms = device_sm_count();
-  if (sms <= 0) return fail(SV_ECUDA, "no CUDA device");
-  const int row_bytes = K * bits / 8;
-  int st = encode_2d(&c.tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, (uint64_t)row_bytes, (uint64_t)N, (uint64_t)row_bytes,
-                     128, BN, CU_TENSOR_MAP_SWIZZLE_128B);
-  if (st) return st;
-  st = encode_2d(&c.ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, scales, (uint64_t)(K / GROUP), (uint64_t)N,
-                 (uint64_t)(K / GROUP) * 2, GPS, BN, CU_TENSOR_MAP_SWIZZLE_NONE);
-  if (st) return st;
-  st = encode_2d(&c.tb, CU_TENSOR_MAP_DATA_TYPE_UINT16, biases, (uint64_t)(K / GROUP), (uint64_t)N,
-                 (uint64_t)(K / GROUP) * 2, GPS, BN, CU_TENSOR_MAP_SWIZZLE_NONE);
-  if (st) return st;
-  QmmParams& p = c.p;
-  memset(&p, 0, sizeof(p));
-  p.sch = make_schedule(N, K, sms);
-  p.M = M;
-  p.MP = 8 * ((M + 7) / 8);
-  const QmmWorkspace L = qmm_workspace_layout(M, N, K, p.sch.grid, with_stats);
-  uint8_t* base = static_cast<uint8_t*>(ws);
-  p.counters = reinterpret_cast<int*>(base + L.counters);
-  p.xp = reinterpret_cast<const __half*>(base + L.xp);
-  p.xsum = reinterpret_cast<const float*>(base + L.xsum);
-  p.rms = reinterpret_cast<const float*>(base + L.rms);
-  p.partials = reinterpret_cast<float*>(base + L.partials);
-  p.tile_stats = with_stats ? reinterpret_cast<float*>(base + L.tile_stats) : nullptr;
   return SV_OK;
 }
 
@@ -180,12 +182,10 @@ static int check_prepare(const uint16_t* x, int ldx, int M, int K, int bits, int
   return SV_OK;
 }
 
-size_t prepare_bytes(int M, int K) { return qmm_workspace_layout(M, 1, K, 0, false).partials; }
+size_t prepare_bytes(int M, int K) { return workspace_layout(M, K, 0, 0, 1).partials; }
 
-int qmm_prepare_internal(const uint16_t* x, int ldx, int M, int K, int bits, int mode, const uint16_t* x2, int ldx2,
-                         const uint16_t* w, float eps, void* ws, cudaStream_t s) {
-  const QmmWorkspace L = qmm_workspace_layout(M, 1, K, 0, false);
-  uint8_t* base = static_cast<uint8_t*>(ws);
+int prepare_into(const uint16_t* x, int ldx, int M, int K, int bits, int mode, const uint16_t* x2, int ldx2,
+                 const uint16_t* w, float eps, const ActBuf& out, cudaStream_t s) {
   PrepArgs a;
   a.x = reinterpret_cast<const __nv_bfloat16*>(x);
   a.ldx = ldx;
@@ -196,45 +196,81 @@ int qmm_prepare_internal(const uint16_t* x, int ldx, int M, int K, int bits, int
   a.M = M;
   a.MP = 8 * ((M + 7) / 8);
   a.K = K;
-  a.xp = reinterpret_cast<__half*>(base + L.xp);
-  a.xsum = reinterpret_cast<float*>(base + L.xsum);
-  a.rms = reinterpret_cast<float*>(base + L.rms);
   a.mode = mode;
+  a.out = out;
   cudaError_t e = launch_prep(a, bits, mode, s);
   if (e != cudaSuccess) return cuda_fail(e, "prepare launch");
   return SV_OK;
+}
+
+int qmm_prepare_internal(const uint16_t* x, int ldx, int M, int K, int bits, int mode, const uint16_t* x2, int ldx2,
+                         const uint16_t* w, float eps, void* ws, cudaStream_t s) {
+  const Layout L = workspace_layout(M, K, 0, 0, 1);
+  return prepare_into(x, ldx, M, K, bits, mode, x2, ldx2, w, eps, act_buf(ws, L, 0), s);
+}
+
+static int grid_for(int bits, int M, int total_units) {
+  const int cap = stream_max_grid(bits, 8 * ((M + 7) / 8));
+  if (cap <= 0) return 0;
+  return total_units < cap ? total_units : cap;
+}
+
+enum RunMode : int { RUN_STORE = 0, RUN_RESIDUAL = 1, RUN_LOGITS = 2 };
+
+size_t qmm_bytes(int M, int N, int K, int bits, bool stats) {
+  const int tiles = (N + BN - 1) / BN;
+  const int grid = grid_for(bits, M, tiles * (K / KC));
+  if (grid <= 0) return 0;
+  return workspace_layout(M, K, grid, stats ? tiles : 0, 1).total;
 }
 
 int qmm_run_internal(const uint32_t* wq, const uint16_t* scales, const uint16_t* biases, int N, int K, int bits,
                      int M, int mode, uint16_t* y, int ldy, const uint16_t* residual, int ldr, float* logits,
                      int ldl, float temperature, float* row_max, float* row_sumexp, int32_t* row_argmax, void* ws,
                      cudaStream_t s) {
-  QmmCall c;
-  const bool stats = mode == EPI_LOGITS;
-  int st = prepare_qmm(c, wq, scales, biases, N, K, bits, M, ws, stats);
+  const int tiles = (N + BN - 1) / BN;
+  const int grid = grid_for(bits, M, tiles * (K / KC));
+  if (grid <= 0) return fail(SV_ECUDA, "no CUDA device");
+  const bool stats = mode == RUN_LOGITS;
+  const Layout L = workspace_layout(M, K, grid, stats ? tiles : 0, 1);
+  static thread_local StreamParams p;  // about 22 KB: kept off the stack
+  stream_params_init(p, ws, L, M, grid, 0.f);
+  int st = encode_weight_maps(p.tm, wq, scales, biases, N, K, bits);
   if (st) return st;
-  c.p.mode = mode;
-  c.p.y = reinterpret_cast<__nv_bfloat16*>(y);
-  c.p.ldy = ldy;
-  c.p.res = reinterpret_cast<const __nv_bfloat16*>(residual);
-  c.p.ldres = ldr;
-  c.p.logits = logits;
-  c.p.ldl = ldl;
-  c.p.inv_temp = temperature > 0.f ? 1.f / temperature : 0.f;
-  cudaError_t e = launch_qmm(bits, c.p.MP / 8, c.tw, c.ts, c.tb, c.p, s);
+  p.maps = nullptr;
+  p.n_phases = 1;
+  Phase& ph = p.ph[0];
+  memset(&ph, 0, sizeof(ph));
+  ph.wq = reinterpret_cast<const uint8_t*>(wq);
+  ph.scales = scales;
+  ph.biases = biases;
+  ph.N = N;
+  ph.K = K;
+  ph.in_buf = 0;
+  ph.out_buf = -1;
+  if (mode == RUN_LOGITS) {
+    ph.kind = PH_LOGITS;
+    p.logits = logits;
+    p.ldl = ldl;
+    p.inv_temp = temperature > 0.f ? 1.f / temperature : 0.f;
+  } else if (mode == RUN_RESIDUAL) {
+    ph.kind = PH_RESID;
+    ph.y = reinterpret_cast<__nv_bfloat16*>(y);
+    ph.ldy = ldy;
+    ph.res = reinterpret_cast<const __nv_bfloat16*>(residual);
+    ph.ldr = ldr;
+  } else {
+    ph.kind = PH_STORE;
+    ph.y = reinterpret_cast<__nv_bfloat16*>(y);
+    ph.ldy = ldy;
+  }
+  cudaError_t e = launch_stream(bits, p, s);
   if (e != cudaSuccess) return cuda_fail(e, "qmm launch");
   if (stats && (row_max || row_sumexp || row_argmax)) {
-    e = launch_lmhead_finalize(c.p.tile_stats, c.p.sch.tiles_n * 2, c.p.MP, M, c.p.inv_temp, row_max, row_sumexp,
-                               row_argmax, s);
+    e = launch_lmhead_finalize(p.tile_stats, tiles, p.MP, M, p.inv_temp, row_max, row_sumexp, row_argmax, s);
     if (e != cudaSuccess) return cuda_fail(e, "lm_head finalize launch");
   }
   return SV_OK;
-}
-
-size_t qmm_bytes(int M, int N, int K, bool stats) {
-  const int sms = device_sm_count();
-  if (sms <= 0) return 0;
-  return qmm_workspace_layout(M, N, K, make_schedule(N, K, sms).grid, stats).total;
 }
 
 }  // namespace sv
@@ -245,12 +281,12 @@ extern "C" {
 
 size_t sv_qmm_workspace_bytes(int M, int N, int K, int bits) {
   if (M < 1 || M > MAX_M || N < 1 || N > MAX_TILES * BN || K < KC || K % KC || (bits != 4 && bits != 8)) return 0;
-  return qmm_bytes(M, N, K, false);
+  return qmm_bytes(M, N, K, bits, false);
 }
 
 size_t sv_lm_head_workspace_bytes(int M, int V, int K, int bits) {
   if (M < 1 || M > MAX_M || V < 1 || V > MAX_TILES * BN || K < KC || K % KC || (bits != 4 && bits != 8)) return 0;
-  return qmm_bytes(M, V, K, true);
+  return qmm_bytes(M, V, K, bits, true);
 }
 
 int sv_qmm_prepare(const uint16_t* x, int ldx, int M, int K, int bits, int mode, const uint16_t* x2, int ldx2,
@@ -270,7 +306,7 @@ static int check_run(const uint32_t* wq, const uint16_t* scales, const uint16_t*
   if (st) return st;
   if (!ws) return fail(SV_EINVAL, "workspace must be non-null");
   if (!aligned(ws, 256)) return fail(SV_EINVAL, "workspace must be 256-byte aligned");
-  const size_t need = qmm_bytes(M, N, K, stats);
+  const size_t need = qmm_bytes(M, N, K, bits, stats);
   if (need == 0) return fail(SV_ECUDA, "no CUDA device");
   if (ws_bytes < need) return fail(SV_EINVAL, "workspace too small: %zu < %zu", ws_bytes, need);
   return SV_OK;
@@ -284,7 +320,7 @@ int sv_qmm_run(const uint32_t* wq, const uint16_t* scales, const uint16_t* biase
   if (!y) return fail(SV_EINVAL, "y must be non-null");
   if (ldy < N || (residual && ldr < N)) return fail(SV_EINVAL, "ldy and ldr must be >= N");
   if (!aligned(y, 2) || (residual && !aligned(residual, 2))) return fail(SV_EINVAL, "misaligned y or residual");
-  return qmm_run_internal(wq, scales, biases, N, K, bits, M, residual ? EPI_BF16_RESIDUAL : EPI_BF16, y, ldy,
+  return qmm_run_internal(wq, scales, biases, N, K, bits, M, residual ? RUN_RESIDUAL : RUN_STORE, y, ldy,
                           residual, ldr, nullptr, 0, 0.f, nullptr, nullptr, nullptr, workspace,
                           static_cast<cudaStream_t>(stream));
 }
@@ -304,7 +340,7 @@ int sv_qmm_verify(const uint32_t* wq, const uint16_t* scales, const uint16_t* bi
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   st = qmm_prepare_internal(x, ldx, M, K, bits, PREP_PLAIN, nullptr, 0, nullptr, 0.f, workspace, s);
   if (st) return st;
-  return qmm_run_internal(wq, scales, biases, N, K, bits, M, residual ? EPI_BF16_RESIDUAL : EPI_BF16, y, ldy,
+  return qmm_run_internal(wq, scales, biases, N, K, bits, M, residual ? RUN_RESIDUAL : RUN_STORE, y, ldy,
                           residual, ldr, nullptr, 0, 0.f, nullptr, nullptr, nullptr, workspace, s);
 }
 
@@ -323,7 +359,7 @@ int sv_lm_head_run(const uint32_t* wq, const uint16_t* scales, const uint16_t* b
   if (st) return st;
   st = check_head_outputs(temperature, logits, ldl, V);
   if (st) return st;
-  return qmm_run_internal(wq, scales, biases, V, K, bits, M, EPI_LOGITS, nullptr, 0, nullptr, 0, logits, ldl,
+  return qmm_run_internal(wq, scales, biases, V, K, bits, M, RUN_LOGITS, nullptr, 0, nullptr, 0, logits, ldl,
                           temperature, row_max, row_sumexp, row_argmax, workspace, static_cast<cudaStream_t>(stream));
 }
 
@@ -342,7 +378,7 @@ int sv_lm_head_verify(const uint32_t* wq, const uint16_t* scales, const uint16_t
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   st = qmm_prepare_internal(x, ldx, M, K, bits, PREP_PLAIN, nullptr, 0, nullptr, 0.f, workspace, s);
   if (st) return st;
-  return qmm_run_internal(wq, scales, biases, V, K, bits, M, EPI_LOGITS, nullptr, 0, nullptr, 0, logits, ldl,
+  return qmm_run_internal(wq, scales, biases, V, K, bits, M, RUN_LOGITS, nullptr, 0, nullptr, 0, logits, ldl,
                           temperature, row_max, row_sumexp, row_argmax, workspace, s);
 }
 

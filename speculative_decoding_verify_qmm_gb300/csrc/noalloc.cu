@@ -57,7 +57,7 @@ int sv_qmm_verify_noalloc(const uint32_t* wq, const uint16_t* scales, const uint
   if (ldx < K || ldy < N || (residual && ldr < N)) return fail(SV_EINVAL, "ldx must be >= K, ldy and ldr >= N");
   if (!aligned(x, 2) || !aligned(y, 2) || (residual && !aligned(residual, 2)))
     return fail(SV_EINVAL, "x, y, residual must be 2-byte aligned");
-  const size_t need = qmm_bytes(M, N, K, false);
+  const size_t need = qmm_bytes(M, N, K, bits, false);
   if (need == 0) return fail(SV_ECUDA, "no CUDA device");
   if (need > NOALLOC_SCRATCH_BYTES)
     return fail(SV_EUNSUPPORTED,
@@ -76,7 +76,7 @@ int sv_qmm_verify_noalloc(const uint32_t* wq, const uint16_t* scales, const uint
   if (e != cudaSuccess) return cuda_fail(e, "clear scratch counters");
   st = qmm_prepare_internal(x, ldx, M, K, bits, PREP_PLAIN, nullptr, 0, nullptr, 0.f, ws, s);
   if (st) return st;
-  return qmm_run_internal(wq, scales, biases, N, K, bits, M, residual ? EPI_BF16_RESIDUAL : EPI_BF16, y, ldy,
+  return qmm_run_internal(wq, scales, biases, N, K, bits, M, residual ? 1 : 0, y, ldy,
                           residual, ldr, nullptr, 0, 0.f, nullptr, nullptr, nullptr, ws, s);
 }
 

@@ -8,6 +8,7 @@
 // The scale is undone once per output row in the epilogue.
 #include "sv_internal.h"
 #include "sv_ptx.cuh"
+#include "stream_kernel.cuh"
 
 namespace sv {
 
@@ -23,64 +24,45 @@ cudaError_t read_and_clear_error_word(unsigned int* out) {
   return e;
 }
 
-// Slot (position in the 32-element block as the MMA fragments read it) of the
-// element at physical offset p within its 32-element block.  The codes are
-// consumed in a permuted k order (see qmm_kernel.cuh); permuting the
-// activations the same way keeps the contraction exact.
-template <int BITS>
-__device__ __forceinline__ int slot_of_phys(int p) {
-  if (BITS == 8) {
-    // slot 8t + i holds element 4t + i (i < 4) or 16 + 4t + (i - 4)
-    const int hi = p >> 4, q = p & 15;
-    return 8 * (q >> 2) + 4 * hi + (q & 3);
-  }
-  // 4-bit: slot 8t + i holds nibble j = (0, 4, 1, 5, 2, 6, 3, 7)[i] of element block 8t
-  const int j = p & 7;
-  return (p & ~7) + (j < 4 ? 2 * j : 2 * (j - 4) + 1);
-}
-
-// One block per (512-wide k chunk, padded row).  Every step is local to the
-// chunk, so the grid covers the whole activation block at once:
+// One warp per (64-wide group, padded row); a block covers 8 groups of one row.
+// Every step is local to the group, so the grid covers the whole block at once:
 //   v   = x, bf16(silu(x) * x2) for SwiGLU, or bf16(x * weight) for RMSNorm
 //         (whose row scale 1/sqrt(mean(x^2) + eps) is applied to the matmul
-//         output; this block stores its chunk's sum of x^2 for that),
-//   e   = 15 - exponent of the chunk's max |v|, so v * 2^e lies below 2^15 and
+//         output from the group sums of x^2 stored here),
+//   e   = 15 - exponent of the group's max |v|, so v * 2^e lies below 2^15 and
 //         every bf16 value keeps all its significant bits in fp16,
-//   out = fp16(v * 2^e) in MMA order, the fp32 sum of each 64-wide group of
-//         v * 2^e, and 2^-e.
+//   out = fp16(v * 2^e) in the order the MMA fragments read the codes, the
+//         fp32 sum of v * 2^e, and 2^-e.
 template <int BITS, int MODE>
 __global__ void __launch_bounds__(256) prep_kernel(PrepArgs a) {
   pdl_trigger();
   pdl_wait();
-  __shared__ float red[8];
-  const int c = blockIdx.x, m = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int m = blockIdx.y, lane = threadIdx.x & 31;
+  const int g = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int MP = a.MP;
   const bool live = m < a.M;
-  const int k0 = c * KC + 2 * tid;  // this thread's two elements
   float v[2] = {0.f, 0.f}, sq = 0.f;
   if (live) {
     const __nv_bfloat16* row = a.x + (size_t)m * a.ldx;
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-      float x = __bfloat162float(row[k0 + i]);
+      const int k = g * GROUP + lane + 32 * i;
+      float x = __bfloat162float(row[k]);
       if (MODE == PREP_RMSNORM) {
         sq = fmaf(x, x, sq);
-        if (a.w) x = __bfloat162float(__float2bfloat16_rn(x * __bfloat162float(a.w[k0 + i])));
+        if (a.w) x = __bfloat162float(__float2bfloat16_rn(x * __bfloat162float(a.w[k])));
       } else if (MODE == PREP_SWIGLU) {
-        const float u = __bfloat162float(a.x2[(size_t)m * a.ldx2 + k0 + i]);
+        const float u = __bfloat162float(a.x2[(size_t)m * a.ldx2 + k]);
         x = __bfloat162float(__float2bfloat16_rn(x / (1.f + expf(-x)) * u));
       }
       v[i] = x;
     }
   }
   float mx = fmaxf(fabsf(v[0]), fabsf(v[1]));
-  for (int off = 16; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-  if (MODE == PREP_RMSNORM)
-    for (int off = 16; off; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
-  if (lane == 0) red[warp] = mx;
-  __syncthreads();
-  mx = red[0];
-#pragma unroll
-  for (int w = 1; w < 8; ++w) mx = fmaxf(mx, red[w]);
+  for (int off = 16; off; off >>= 1) {
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    sq += __shfl_xor_sync(0xffffffffu, sq, off);
+  }
   int e = 0;
   if (mx > 0.f && mx <= 3.0e38f) {
     int E;
@@ -92,27 +74,19 @@ __global__ void __launch_bounds__(256) prep_kernel(PrepArgs a) {
   float gs = 0.f;
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
-    const int k = 2 * tid + i;  // offset within the chunk
+    const int p = lane;  // element lane + 32 i of the group: block 2g + i, offset lane
     const float y = v[i] * sc;
     gs += y;
-    a.xp[((size_t)(c * (KC / 32) + (k >> 5)) * a.MP + m) * 32 + slot_of_phys<BITS>(k & 31)] = __float2half_rn(y);
+    a.out.xp[((size_t)(2 * g + i) * MP + m) * 32 + slot_of_phys<BITS>(p)] = __float2half_rn(y);
   }
-  // warp w covers elements 64w .. 64w+63 of the chunk: exactly group w
   for (int off = 16; off; off >>= 1) gs += __shfl_xor_sync(0xffffffffu, gs, off);
-  float* xs = a.xsum + (size_t)c * (GPS + 1) * a.MP;
-  if (lane == 0) xs[warp * a.MP + m] = gs;
-  if (tid == 0) xs[GPS * a.MP + m] = live ? ldexpf(1.f, -e) : 0.f;
-  if (MODE == PREP_RMSNORM) {
-    __syncthreads();
-    if (lane == 0) red[warp] = sq;
-    __syncthreads();
-    if (tid == 0) {
-      float t = 0.f;
-      for (int w = 0; w < 8; ++w) t += red[w];
-      a.rms[(size_t)c * a.MP + m] = t;
-    }
+  if (lane == 0) {
+    float* xs = a.out.xs + (size_t)g * 2 * MP;
+    xs[m] = gs;
+    xs[MP + m] = ldexpf(1.f, -e);
+    a.out.sq[(size_t)g * MP + m] = sq;
+    if (g == 0) a.out.sq[(size_t)(a.K / GROUP) * MP + m] = MODE == PREP_RMSNORM ? a.eps : -1.f;
   }
-  if (c == 0 && tid == 0) a.rms[(size_t)(a.K / KC) * a.MP + m] = MODE == PREP_RMSNORM ? a.eps : -1.f;
 }
 
 cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, size_t smem, cudaStream_t s, cudaLaunchAttribute* attr) {

@@ -4,20 +4,24 @@
 // through one forward and the accept step commits the longest accepted
 // prefix.  The layer body is the plainest dense block (the pages give none):
 //
-//   a  = RMSNorm(h)                    fused into the preparation of qkv's input
-//   qkv = a Wqkv^T                      q | k | v in one weight stream
-//   h += q Wo^T                         q feeds o directly (no attention state)
-//   a2 = RMSNorm(h)                    fused into the preparation of gate|up's input
-//   gu = a2 Wgu^T                       gate | up in one weight stream
-//   h += (silu(g) * u) Wdown^T          SwiGLU fused into the preparation of down's input
+//   qkv = RMSNorm(h) Wqkv^T            q | k | v in one weight stream
+//   h  += q Wo^T                        q feeds o directly (no attention state)
+//   gu  = RMSNorm(h) Wgu^T              gate / up rows interleaved in 64-row blocks
+//   h  += (silu(gate) * up) Wdown^T
 //
-// then a = RMSNorm(h), the vocab head with its row statistics, and the accept
-// step.  Every launch carries the programmatic-serialization attribute, so a
-// projection's weight stream starts while the previous kernel drains; the
-// whole sequence can be captured into one CUDA graph by the caller.
+// then logits = RMSNorm(h) Wlm^T with row statistics, and the accept step.
+// All 4 * layers + 1 projections run as the phases of one persistent launch:
+// each phase's epilogue prepares the next phase's input (the RMSNorm row scale
+// is applied to the consuming projection's output), so nothing runs between
+// projections but a grid-wide barrier, behind which the next weights already
+// stream.  Launches: input preparation, the phases, the row-statistics merge,
+// the accept step.
 #include <algorithm>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
+#include <unordered_map>
+#include <vector>
 
 #include "sv_internal.h"
 #include "sv_kernels.h"
@@ -25,27 +29,24 @@
 namespace sv {
 
 struct RoundLayout {
+  Layout ws;
   size_t stats, qkv, gu, total;
+  int grid;
 };
 
-static RoundLayout round_layout(const sv_model* md, int rows, bool& ok) {
-  ok = false;
-  RoundLayout L = {};
-  const int K_h = md->hidden;
-  const size_t qmm = std::max({qmm_bytes(rows, md->layers[0].qkv.N, K_h, false),
-                               qmm_bytes(rows, md->hidden, md->q_dim, false),
-                               qmm_bytes(rows, 2 * md->inter, K_h, false),
-                               qmm_bytes(rows, md->hidden, md->inter, false),
-                               qmm_bytes(rows, md->vocab, K_h, true)});
-  if (qmm == 0) return L;
-  const size_t acc = accept_bytes(rows, rows);
-  size_t off = align256(std::max(qmm, acc));
-  L.stats = off; off = align256(off + (size_t)rows * 12);
-  L.qkv = off;   off = align256(off + (size_t)rows * md->layers[0].qkv.N * 2);
-  L.gu = off;    off = align256(off + (size_t)rows * 2 * md->inter * 2);
-  L.total = off;
-  ok = true;
-  return L;
+static bool round_layout(const sv_model* md, int rows, RoundLayout& R) {
+  const int MP = 8 * ((rows + 7) / 8);
+  R.grid = stream_max_grid(md->bits, MP);
+  if (R.grid <= 0) return false;
+  const int K_cap = std::max({md->hidden, md->q_dim, md->inter});
+  const int vocab_tiles = (md->vocab + BN - 1) / BN;
+  R.ws = workspace_layout(rows, K_cap, R.grid, vocab_tiles, 2);
+  size_t off = align256(std::max(R.ws.total, accept_bytes(rows, rows)));
+  R.stats = off; off = align256(off + (size_t)rows * 12);
+  R.qkv = off;   off = align256(off + (size_t)rows * md->layers[0].qkv.N * 2);
+  R.gu = off;    off = align256(off + (size_t)rows * 2 * md->inter * 2);
+  R.total = off;
+  return true;
 }
 
 static int check_proj(const sv_qweight& w, int N, int K, int bits, int M, const char* what, int layer) {
@@ -63,6 +64,7 @@ static int check_proj(const sv_qweight& w, int N, int K, int bits, int M, const 
 static int check_model(const sv_model* md, int M) {
   if (!md || !md->layers) return fail(SV_EINVAL, "model and its layer array must be non-null");
   if (md->n_layers < 1) return fail(SV_EINVAL, "n_layers must be >= 1");
+  if (4 * md->n_layers + 1 > MAX_PHASES) return fail(SV_EUNSUPPORTED, "at most %d layers", (MAX_PHASES - 1) / 4);
   if (md->bits != 4 && md->bits != 8) return fail(SV_EUNSUPPORTED, "bits must be 4 or 8");
   if (md->hidden < 1 || md->q_dim < 1 || md->inter < 1 || md->vocab < 2)
     return fail(SV_EINVAL, "model dimensions must be positive");
@@ -80,6 +82,44 @@ static int check_model(const sv_model* md, int M) {
   return check_proj(md->lm_head, md->vocab, md->hidden, md->bits, M, "lm_head", -1);
 }
 
+static void set_phase(Phase& ph, const sv_qweight& w, int kind, int in_buf, int out_buf) {
+  memset(&ph, 0, sizeof(ph));
+  ph.wq = reinterpret_cast<const uint8_t*>(w.wq);
+  ph.scales = w.scales;
+  ph.biases = w.biases;
+  ph.N = w.N;
+  ph.K = w.K;
+  ph.kind = kind;
+  ph.in_buf = in_buf;
+  ph.out_buf = out_buf;
+}
+
+// A plan holds the tensor maps (weights, scales, biases) of every projection
+// of a model, in phase order, in device memory: the persistent kernel reads a
+// phase's maps from there, so they are encoded once per model instead of once
+// per round.  The host remembers which model each plan was built for.
+static uint64_t mix(uint64_t h, uint64_t v) { return (h ^ v) * 0x100000001b3ull; }  // FNV-1a over 64-bit words
+static uint64_t hash_qweight(uint64_t h, const sv_qweight& w) {
+  h = mix(h, reinterpret_cast<uintptr_t>(w.wq));
+  h = mix(h, reinterpret_cast<uintptr_t>(w.scales));
+  h = mix(h, reinterpret_cast<uintptr_t>(w.biases));
+  return mix(h, ((uint64_t)(uint32_t)w.N << 32) | (uint32_t)w.K);
+}
+static uint64_t model_fingerprint(const sv_model* md) {
+  uint64_t h = 0xcbf29ce484222325ull;
+  const int dims[6] = {md->n_layers, md->hidden, md->q_dim, md->inter, md->vocab, md->bits};
+  for (int d : dims) h = mix(h, (uint32_t)d);
+  for (int l = 0; l < md->n_layers; ++l) {
+    const sv_layer& L = md->layers[l];
+    h = hash_qweight(hash_qweight(hash_qweight(hash_qweight(h, L.qkv), L.o), L.gate_up), L.down);
+  }
+  return hash_qweight(h, md->lm_head);
+}
+static std::mutex g_plan_mu;
+static std::unordered_map<const void*, uint64_t> g_plans;
+
+static size_t plan_bytes_for(const sv_model* md) { return (size_t)(4 * md->n_layers + 1) * 3 * sizeof(CUtensorMap); }
+
 }  // namespace sv
 
 using namespace sv;
@@ -88,15 +128,45 @@ extern "C" {
 
 size_t sv_round_workspace_bytes(const sv_model* model, int rows) {
   if (!model || !model->layers || model->n_layers < 1 || rows < 1 || rows > MAX_M) return 0;
-  bool ok;
-  RoundLayout L = round_layout(model, rows, ok);
-  return ok ? L.total : 0;
+  RoundLayout R;
+  return round_layout(model, rows, R) ? R.total : 0;
 }
 
-int sv_verify_round(const sv_model* model, int B, const int32_t* row_offsets, uint16_t* hidden, int ldh,
+size_t sv_round_plan_bytes(const sv_model* model) {
+  if (!model || !model->layers || model->n_layers < 1 || 4 * model->n_layers + 1 > MAX_PHASES) return 0;
+  return plan_bytes_for(model);
+}
+
+int sv_round_plan_init(const sv_model* model, void* plan, size_t plan_bytes) {
+  int st = check_model(model, 1);
+  if (st) return st;
+  if (!plan || !aligned(plan, 256)) return fail(SV_EINVAL, "plan must be non-null and 256-byte aligned");
+  const size_t need = plan_bytes_for(model);
+  if (plan_bytes < need) return fail(SV_EINVAL, "plan too small: %zu < %zu", plan_bytes, need);
+  std::vector<CUtensorMap> maps((size_t)(4 * model->n_layers + 1) * 3);
+  size_t n = 0;
+  auto add = [&](const sv_qweight& w) {
+    CUtensorMap m3[3];
+    int r = encode_weight_maps(m3, w.wq, w.scales, w.biases, w.N, w.K, model->bits);
+    for (int i = 0; i < 3; ++i) maps[n++] = m3[i];
+    return r;
+  };
+  for (int l = 0; l < model->n_layers; ++l) {
+    const sv_layer& L = model->layers[l];
+    if ((st = add(L.qkv)) || (st = add(L.o)) || (st = add(L.gate_up)) || (st = add(L.down))) return st;
+  }
+  if ((st = add(model->lm_head))) return st;
+  cudaError_t e = cudaMemcpy(plan, maps.data(), need, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(e, "copy plan to the device");
+  std::lock_guard<std::mutex> lock(g_plan_mu);
+  g_plans[plan] = model_fingerprint(model);
+  return SV_OK;
+}
+
+int sv_verify_round(const sv_model* model, const void* plan, int B, const int32_t* row_offsets, uint16_t* hidden, int ldh,
                     float temperature, const float* q, int ldq, const int32_t* draft, const float* u, float* logits,
                     int ldl, int32_t* out_len, int32_t* out_tokens, void* workspace, size_t workspace_bytes,
-                    void* stream) {
+                    void* stream, void* event_start, void* event_stop) {
   if (B < 1 || !row_offsets) return fail(SV_EINVAL, "B must be >= 1 with row offsets");
   const int M = row_offsets[B];
   if (M < 1 || M > MAX_M) return fail(M > MAX_M ? SV_EUNSUPPORTED : SV_EINVAL, "total rows %d not in [1, 32]", M);
@@ -106,50 +176,74 @@ int sv_verify_round(const sv_model* model, int B, const int32_t* row_offsets, ui
                     u, out_len, out_tokens);
   if (st) return st;
   if (!hidden || ldh < model->hidden || !aligned(hidden, 2)) return fail(SV_EINVAL, "bad hidden-state buffer");
+  {
+    std::lock_guard<std::mutex> lock(g_plan_mu);
+    auto it = g_plans.find(plan);
+    if (!plan || it == g_plans.end() || it->second != model_fingerprint(model))
+      return fail(SV_EINVAL, "plan was not built for this model (sv_round_plan_init)");
+  }
   if (!workspace || !aligned(workspace, 256)) return fail(SV_EINVAL, "workspace must be non-null, 256-byte aligned");
-  bool ok;
-  const RoundLayout L = round_layout(model, M, ok);
-  if (!ok) return fail(SV_ECUDA, "no CUDA device");
-  if (workspace_bytes < L.total) return fail(SV_EINVAL, "workspace too small: %zu < %zu", workspace_bytes, L.total);
+  RoundLayout R;
+  if (!round_layout(model, M, R)) return fail(SV_ECUDA, "no CUDA device");
+  if (workspace_bytes < R.total) return fail(SV_EINVAL, "workspace too small: %zu < %zu", workspace_bytes, R.total);
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* base = static_cast<uint8_t*>(workspace);
-  uint16_t* qkv = reinterpret_cast<uint16_t*>(base + L.qkv);
-  uint16_t* gu = reinterpret_cast<uint16_t*>(base + L.gu);
-  float* rmax = reinterpret_cast<float*>(base + L.stats);
+  __nv_bfloat16* qkv = reinterpret_cast<__nv_bfloat16*>(base + R.qkv);
+  __nv_bfloat16* gu = reinterpret_cast<__nv_bfloat16*>(base + R.gu);
+  __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(hidden);
+  float* rmax = reinterpret_cast<float*>(base + R.stats);
   float* rsum = rmax + M;
   int32_t* rarg = reinterpret_cast<int32_t*>(rsum + M);
-  const int H = model->hidden, Dq = model->q_dim, I = model->inter, bits = model->bits;
-  const int Nqkv = model->layers[0].qkv.N;
-  const float eps = model->rms_eps;
-#define SV_TRY(x)            \
-  do {                       \
-    int st_ = (x);           \
-    if (st_) return st_;     \
-  } while (0)
+  const int bits = model->bits, Nqkv = model->layers[0].qkv.N, I = model->inter;
+
+  static thread_local StreamParams p;  // about 22 KB: kept off the stack
+  stream_params_init(p, workspace, R.ws, M, R.grid, model->rms_eps);
+  p.maps = static_cast<const CUtensorMap*>(plan);
+  int n = 0;
   for (int l = 0; l < model->n_layers; ++l) {
     const sv_layer& W = model->layers[l];
-    SV_TRY(qmm_prepare_internal(hidden, ldh, M, H, bits, PREP_RMSNORM, nullptr, 0, nullptr, eps, workspace, s));
-    SV_TRY(qmm_run_internal(W.qkv.wq, W.qkv.scales, W.qkv.biases, Nqkv, H, bits, M, EPI_BF16, qkv, Nqkv, nullptr, 0,
-                            nullptr, 0, 0.f, nullptr, nullptr, nullptr, workspace, s));
-    SV_TRY(qmm_prepare_internal(qkv, Nqkv, M, Dq, bits, PREP_PLAIN, nullptr, 0, nullptr, 0.f, workspace, s));
-    SV_TRY(qmm_run_internal(W.o.wq, W.o.scales, W.o.biases, H, Dq, bits, M, EPI_BF16_RESIDUAL, hidden, ldh, hidden,
-                            ldh, nullptr, 0, 0.f, nullptr, nullptr, nullptr, workspace, s));
-    SV_TRY(qmm_prepare_internal(hidden, ldh, M, H, bits, PREP_RMSNORM, nullptr, 0, nullptr, eps, workspace, s));
-    SV_TRY(qmm_run_internal(W.gate_up.wq, W.gate_up.scales, W.gate_up.biases, 2 * I, H, bits, M, EPI_BF16, gu, 2 * I,
-                            nullptr, 0, nullptr, 0, 0.f, nullptr, nullptr, nullptr, workspace, s));
-    SV_TRY(qmm_prepare_internal(gu, 2 * I, M, I, bits, PREP_SWIGLU, gu + I, 2 * I, nullptr, 0.f, workspace, s));
-    SV_TRY(qmm_run_internal(W.down.wq, W.down.scales, W.down.biases, H, I, bits, M, EPI_BF16_RESIDUAL, hidden, ldh,
-                            hidden, ldh, nullptr, 0, 0.f, nullptr, nullptr, nullptr, workspace, s));
+    Phase& a = p.ph[n++];
+    set_phase(a, W.qkv, PH_STORE, 0, 1);
+    a.y = qkv;
+    a.ldy = Nqkv;
+    a.prep_tiles = model->q_dim / BN;
+    Phase& o = p.ph[n++];
+    set_phase(o, W.o, PH_RESID, 1, 0);
+    o.y = h;
+    o.res = h;
+    o.ldy = o.ldr = ldh;
+    Phase& g = p.ph[n++];
+    set_phase(g, W.gate_up, PH_GATEUP, 0, 1);
+    g.y = gu;
+    g.ldy = 2 * I;
+    g.half = I;
+    Phase& d = p.ph[n++];
+    set_phase(d, W.down, PH_RESID, 1, 0);
+    d.y = h;
+    d.res = h;
+    d.ldy = d.ldr = ldh;
   }
-  SV_TRY(qmm_prepare_internal(hidden, ldh, M, H, bits, PREP_RMSNORM, nullptr, 0, nullptr, eps, workspace, s));
-  SV_TRY(qmm_run_internal(model->lm_head.wq, model->lm_head.scales, model->lm_head.biases, model->vocab, H, bits, M,
-                          EPI_LOGITS, nullptr, 0, nullptr, 0, logits, ldl, temperature, rmax, rsum, rarg, workspace,
-                          s));
-  SV_TRY(accept_internal(B, row_offsets, logits, ldl, rmax, temperature > 0.f ? rsum : nullptr, rarg, q, ldq, draft,
-                         model->vocab, temperature, u, out_len, out_tokens, workspace, s));
-#undef SV_TRY
-  return SV_OK;
+  set_phase(p.ph[n++], model->lm_head, PH_LOGITS, 0, -1);
+  p.n_phases = n;
+  p.logits = logits;
+  p.ldl = ldl;
+  p.inv_temp = temperature > 0.f ? 1.f / temperature : 0.f;
+
+  st = prepare_into(hidden, ldh, M, model->hidden, bits, PREP_RMSNORM, nullptr, 0, nullptr, model->rms_eps, p.act[0],
+                    s);
+  if (st) return st;
+  cudaError_t e;
+  if (event_start && (e = cudaEventRecord(static_cast<cudaEvent_t>(event_start), s)) != cudaSuccess)
+    return cuda_fail(e, "record event_start");
+  e = launch_stream(bits, p, s);
+  if (e != cudaSuccess) return cuda_fail(e, "verify-round launch");
+  if (event_stop && (e = cudaEventRecord(static_cast<cudaEvent_t>(event_stop), s)) != cudaSuccess)
+    return cuda_fail(e, "record event_stop");
+  e = launch_lmhead_finalize(p.tile_stats, (model->vocab + BN - 1) / BN, p.MP, M, p.inv_temp, rmax, rsum, rarg, s);
+  if (e != cudaSuccess) return cuda_fail(e, "lm_head finalize launch");
+  return accept_internal(B, row_offsets, logits, ldl, rmax, temperature > 0.f ? rsum : nullptr, rarg, q, ldq, draft,
+                         model->vocab, temperature, u, out_len, out_tokens, workspace, s);
 }
 
 }  // extern "C"

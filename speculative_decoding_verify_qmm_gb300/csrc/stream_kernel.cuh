@@ -1,0 +1,936 @@
+// Persistent multi-phase verify matmul.
+//
+// One launch runs a sequence of "phases"; each phase is one skinny
+// affine-group-quantized matmul of the verify round (a q|k|v, o, gate|up, down
+// or vocab-head projection):
+//
+//     Y[m, n] = sum_k X[m, k] * (scale[n, k/64] * code[n, k] + bias[n, k/64]),  M <= 32 rows.
+//
+// mlx-dspark wiki page, "Key techniques": the verify kernel dequantizes each
+// weight group once and reuses it across all rows.  Here that is a factored
+// form evaluated per group g and weight row n,
+//
+//     Y[m, n] += scale[n,g] * sum_{k in g} X[m,k] * (code[n,k] - off)  +  (bias[n,g] + off*scale[n,g]) * sum_{k in g} X[m,k]
+//
+// with the inner sums on the tensor cores (codes are exact small integers in
+// fp16, `off` = 128 or 8 centres them) and the two group terms in fp32, so no
+// weight is ever rounded to a 16-bit float.  Activations arrive as fp16 scaled
+// by 2^e per (row, group) so that every bf16 value keeps all its bits.
+//
+// Work and data flow (one CTA per SM, stream-K over (64-row tile, 512-k chunk)
+// units of every phase, so every SM streams the same number of weight bytes):
+//   * warp 8 (producer) fills a ring of shared-memory stages with TMA copies:
+//     the tile's codes as 64-row x 128-byte boxes with the 128-byte swizzle
+//     (ldmatrix then reads them without bank conflicts), one 64 x 8 box each
+//     of scales and biases, and the matching slice of the prepared
+//     activations as plain bulk copies.  It runs ahead into the next phase's
+//     weights while the current phase drains; only the activation copies wait
+//     for the grid-wide phase barrier.
+//   * warps 0-7 (consumers) are 4 row quarters x 2 k halves: ldmatrix the codes,
+//     turn them into fp16 with byte-permute / LOP3, mma.sync m16n8k16 against
+//     the activation fragments, fold each group into fp32 sums.  At a tile's
+//     end the two k halves are added (fixed order) into one of two result
+//     slots in shared memory, and the consumers go straight on to the next
+//     unit: nothing that waits on global memory runs on them.
+//   * warps 9-12 (epilogue, one per row quarter) finish each tile from its
+//     result slot.  A tile split across CTAs is finished by whichever
+//     contributor arrives last (atomic counter, no spinning), adding the
+//     partials in CTA order, so results are bitwise reproducible.  The
+//     finishing epilogue writes the phase output and prepares it as the next
+//     phase's input (fp16 scaling, group sums, RMSNorm statistics, SwiGLU of
+//     gate/up block pairs).
+//   * between phases the last epilogue warp of every CTA to finish the phase
+//     arrives on a grid counter; the producer issues the next phase's
+//     activation copies once all CTAs have arrived.  Every wait is bounded
+//     (about 2 s) and ends in an error flag, never in a hang.
+#pragma once
+
+#include "sv_internal.h"
+#include "sv_ptx.cuh"
+
+namespace sv {
+
+template <int BITS, int NT>
+struct StreamCfg {
+  static constexpr int MP = 8 * NT;
+  static constexpr int ROW_BYTES = KC * BITS / 8;  // code bytes per weight row per stage
+  static constexpr int ATOMS = ROW_BYTES / 128;    // 128-byte swizzled boxes per stage
+  static constexpr int W_BYTES = BN * ROW_BYTES;
+  static constexpr int X_BYTES = MP * KC * 2;
+  static constexpr int XS_BYTES = GPS * 2 * MP * 4;  // per group: scaled sums, then 2^-e
+  static constexpr int SB_BYTES = BN * GPS * 2;
+  static constexpr int X_OFF = W_BYTES;
+  static constexpr int XS_OFF = X_OFF + X_BYTES;
+  static constexpr int S_OFF = (XS_OFF + XS_BYTES + 127) / 128 * 128;
+  static constexpr int B_OFF = S_OFF + SB_BYTES;
+  static constexpr int TX_BYTES = W_BYTES + X_BYTES + XS_BYTES + 2 * SB_BYTES;  // full boxes, ragged tiles too
+  static constexpr int STAGE_BYTES = (B_OFF + SB_BYTES + 1023) / 1024 * 1024;  // swizzle atoms 1024-aligned
+  static constexpr int RED_FLOATS = 16 * MP;        // one quarter's 16 rows
+  static constexpr int RED_BYTES = 2 * 4 * RED_FLOATS * 4;  // result slot x quarter
+  static constexpr int EPI_BYTES = 4 * 4 * MP * 4 + 256;    // cross-quarter scratch
+  static constexpr int BUDGET = 227 * 1024 - 1024 - 2048 - RED_BYTES - EPI_BYTES;
+  static constexpr int STAGES_FIT = BUDGET / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + RED_BYTES + EPI_BYTES;
+  static_assert(STAGES >= 2, "stage ring too small");
+  static_assert(SMEM + 2048 <= 227 * 1024, "shared memory budget");
+  static_assert(W_BYTES % 1024 == 0 && X_OFF % 16 == 0 && XS_OFF % 16 == 0 && S_OFF % 128 == 0 &&
+                    B_OFF % 128 == 0, "copy destination alignment");
+};
+
+// ------------------------------------------------------------ schedule math
+__device__ __forceinline__ int ph_units(const Phase& ph) { return ((ph.N + BN - 1) / BN) * (ph.K / KC); }
+__device__ __forceinline__ int unit_start(int c, int total, int grid) {
+  return static_cast<int>(static_cast<long long>(c) * total / grid);
+}
+__device__ __forceinline__ int unit_owner(long long u, int total, int grid) {
+  return static_cast<int>(((u + 1) * grid - 1) / total);
+}
+
+// Walks this CTA's units phase by phase, in the order both producer and
+// consumers process them.
+struct UnitIter {
+  int phase, u, u_end, total;
+  __device__ __forceinline__ void start(const StreamParams& p, int ph_from) {
+    phase = ph_from - 1;
+    u = u_end = 0;
+    advance_phase(p);
+  }
+  __device__ __forceinline__ void advance_phase(const StreamParams& p) {
+    do {
+      ++phase;
+      if (phase >= p.n_phases) return;
+      total = ph_units(p.ph[phase]);
+      u = unit_start(blockIdx.x, total, p.grid);
+      u_end = unit_start(blockIdx.x + 1, total, p.grid);
+    } while (u >= u_end);
+  }
+  __device__ __forceinline__ bool done(const StreamParams& p) const { return phase >= p.n_phases; }
+  __device__ __forceinline__ void next(const StreamParams& p) {
+    if (++u >= u_end) advance_phase(p);
+  }
+};
+
+// ---------------------------------------------------------- code conversion
+// fp16 pair (1024 + c0, 1024 + c1) from two code bytes, then centred: (c0 - 128, c1 - 128).
+__device__ __forceinline__ uint32_t cvt8(uint32_t codes, uint32_t sel) {
+  uint32_t v = __byte_perm(codes, 0x64646464u, sel);
+  __half2 h = __hadd2(*reinterpret_cast<__half2*>(&v), __half2half2(__ushort_as_half(0xE480)));  // -1152
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+// Four fp16 pairs (n - 8) from the eight 4-bit codes of one word; nibble j is element 8t + j.
+// P0 = (n0, n4), P1 = (n1, n5), P2 = (n2, n6), P3 = (n3, n7).
+__device__ __forceinline__ void cvt4(uint32_t w, uint32_t (&P)[4]) {
+  const __half2 sub = __half2half2(__ushort_as_half(0xE408));        // -1032
+  const __half2 sixteenth = __half2half2(__ushort_as_half(0x2C00));  // 1/16
+  const __half2 sub_hi = __half2half2(__ushort_as_half(0xD480));     // -72
+  uint32_t lo = (w & 0x000F000Fu) | 0x64006400u;
+  uint32_t hi = (w & 0x00F000F0u) | 0x64006400u;
+  uint32_t w8 = w >> 8;
+  uint32_t lo2 = (w8 & 0x000F000Fu) | 0x64006400u;
+  uint32_t hi2 = (w8 & 0x00F000F0u) | 0x64006400u;
+  __half2 r0 = __hadd2(*reinterpret_cast<__half2*>(&lo), sub);
+  __half2 r1 = __hfma2(*reinterpret_cast<__half2*>(&hi), sixteenth, sub_hi);
+  __half2 r2 = __hadd2(*reinterpret_cast<__half2*>(&lo2), sub);
+  __half2 r3 = __hfma2(*reinterpret_cast<__half2*>(&hi2), sixteenth, sub_hi);
+  P[0] = *reinterpret_cast<uint32_t*>(&r0);
+  P[1] = *reinterpret_cast<uint32_t*>(&r1);
+  P[2] = *reinterpret_cast<uint32_t*>(&r2);
+  P[3] = *reinterpret_cast<uint32_t*>(&r3);
+}
+
+// Slot of the element at physical offset p (0..31) of a 32-element activation
+// block, in the order the MMA fragments read the codes.
+template <int BITS>
+__device__ __forceinline__ int slot_of_phys(int p) {
+  if (BITS == 8) {  // slot 8t + i holds element 4t + i (i < 4) or 16 + 4t + (i - 4)
+    const int hi = p >> 4, q = p & 15;
+    return 8 * (q >> 2) + 4 * hi + (q & 3);
+  }
+  const int j = p & 7;  // 4-bit: slot 8t + i holds nibble (0, 4, 1, 5, 2, 6, 3, 7)[i] of block 8t
+  return (p & ~7) + (j < 4 ? 2 * j : 2 * (j - 4) + 1);
+}
+
+template <int NT>
+__device__ __forceinline__ void zero4(float (&a)[NT][4]) {
+#pragma unroll
+  for (int j = 0; j < NT; ++j) a[j][0] = a[j][1] = a[j][2] = a[j][3] = 0.f;
+}
+
+// One consumer warp's share of one stage: groups 4kh .. 4kh+3 for rows 16q .. 16q+15.
+template <int BITS, int NT>
+__device__ __forceinline__ void consume_stage(const uint8_t* st, int q, int kh, int lane, float (&tot)[NT][4]) {
+  using C = StreamCfg<BITS, NT>;
+  constexpr int MP = C::MP;
+  constexpr float OFF = BITS == 8 ? 128.f : 8.f;
+  const int gid = lane >> 2, t = lane & 3;
+  const uint32_t w_base = smem_u32(st);
+  const uint32_t x_base = smem_u32(st + C::X_OFF);
+  const float* xs = reinterpret_cast<const float*>(st + C::XS_OFF);
+  const __half* sc = reinterpret_cast<const __half*>(st + C::S_OFF);  // [64][8]
+  const __half* bi = reinterpret_cast<const __half*>(st + C::B_OFF);
+  const int mi = lane >> 3, rr = lane & 7;  // ldmatrix: matrix mi (row half mi&1, chunk +mi>>1), row rr
+  const int lrow = 16 * q + (mi & 1) * 8 + rr;
+  // row lrow of a 128-byte swizzled box: 16-byte chunk c sits at c ^ (lrow & 7) = c ^ rr
+  const uint32_t arow = w_base + lrow * 128;
+  // this warp's four groups of scales / biases for its rows gid and gid + 8
+  float s_v[2][4], b_v[2][4];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int n = 16 * q + gid + 8 * h;
+    const uint2 s4 = *reinterpret_cast<const uint2*>(sc + n * GPS + 4 * kh);
+    const uint2 b4 = *reinterpret_cast<const uint2*>(bi + n * GPS + 4 * kh);
+    const __half2 s01 = *reinterpret_cast<const __half2*>(&s4.x), s23 = *reinterpret_cast<const __half2*>(&s4.y);
+    const __half2 b01 = *reinterpret_cast<const __half2*>(&b4.x), b23 = *reinterpret_cast<const __half2*>(&b4.y);
+    s_v[h][0] = __low2float(s01);
+    s_v[h][1] = __high2float(s01);
+    s_v[h][2] = __low2float(s23);
+    s_v[h][3] = __high2float(s23);
+    b_v[h][0] = fmaf(OFF, s_v[h][0], __low2float(b01));
+    b_v[h][1] = fmaf(OFF, s_v[h][1], __high2float(b01));
+    b_v[h][2] = fmaf(OFF, s_v[h][2], __low2float(b23));
+    b_v[h][3] = fmaf(OFF, s_v[h][3], __high2float(b23));
+  }
+#pragma unroll
+  for (int gi = 0; gi < 4; ++gi) {
+    const int gl = 4 * kh + gi;  // group index within the stage
+    uint32_t bfr[2][NT][4];
+#pragma unroll
+    for (int blk = 0; blk < 2; ++blk)
+#pragma unroll
+      for (int j = 0; j < NT; ++j)
+        lds128(bfr[blk][j], x_base + ((((gl * 2 + blk) * MP + 8 * j + gid) * 32 + 8 * t) * 2));
+    float acc[NT][4];
+    zero4<NT>(acc);
+    if constexpr (BITS == 8) {
+      // box gl/2 holds groups 2(gl/2), 2(gl/2)+1; a group is 4 chunks (one k16 step each)
+      uint32_t qd[2][4];
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        ldsm_x4(qd[h], arow + (gl >> 1) * (BN * 128) + (((4 * (gl & 1) + 2 * h + (mi >> 1)) ^ rr) << 4));
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        const uint32_t lo = qd[s >> 1][(s & 1) * 2], hi = qd[s >> 1][(s & 1) * 2 + 1];
+        uint32_t a[4] = {cvt8(lo, 0x4140u), cvt8(hi, 0x4140u), cvt8(lo, 0x4342u), cvt8(hi, 0x4342u)};
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+          mma_16816(acc[j], a, bfr[s >> 1][j][(s & 1) * 2], bfr[s >> 1][j][(s & 1) * 2 + 1]);
+      }
+    } else {
+      // box gl/4 holds groups 4(gl/4) .. +3; a group is 2 chunks
+      uint32_t qd[4];
+      ldsm_x4(qd, arow + (gl >> 2) * (BN * 128) + (((2 * (gl & 3) + (mi >> 1)) ^ rr) << 4));
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t Plo[4], Phi[4];
+        cvt4(qd[2 * c], Plo);
+        cvt4(qd[2 * c + 1], Phi);
+        uint32_t a0[4] = {Plo[0], Phi[0], Plo[1], Phi[1]};
+        uint32_t a1[4] = {Plo[2], Phi[2], Plo[3], Phi[3]};
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          mma_16816(acc[j], a0, bfr[c][j][0], bfr[c][j][1]);
+          mma_16816(acc[j], a1, bfr[c][j][2], bfr[c][j][3]);
+        }
+      }
+    }
+    // tot += 2^-e * (s * acc + (b + off*s) * xsum)
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      const float2 xsv = *reinterpret_cast<const float2*>(xs + (gl * 2) * MP + 8 * j + 2 * t);
+      const float2 fv = *reinterpret_cast<const float2*>(xs + (gl * 2 + 1) * MP + 8 * j + 2 * t);
+      tot[j][0] = fmaf(fv.x, fmaf(s_v[0][gi], acc[j][0], b_v[0][gi] * xsv.x), tot[j][0]);
+      tot[j][1] = fmaf(fv.y, fmaf(s_v[0][gi], acc[j][1], b_v[0][gi] * xsv.y), tot[j][1]);
+      tot[j][2] = fmaf(fv.x, fmaf(s_v[1][gi], acc[j][2], b_v[1][gi] * xsv.x), tot[j][2]);
+      tot[j][3] = fmaf(fv.y, fmaf(s_v[1][gi], acc[j][3], b_v[1][gi] * xsv.y), tot[j][3]);
+    }
+  }
+}
+
+template <int NT>
+__device__ __forceinline__ void red_store(float* buf, const float (&v)[NT][4], int lane) {
+#pragma unroll
+  for (int j = 0; j < NT; ++j)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) buf[(j * 4 + e) * 32 + lane] = v[j][e];
+}
+template <int NT, bool GLOBAL>
+__device__ __forceinline__ void red_add(const float* buf, float (&v)[NT][4], int lane) {
+#pragma unroll
+  for (int j = 0; j < NT; ++j)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float* a = buf + (j * 4 + e) * 32 + lane;
+      v[j][e] += GLOBAL ? __ldcg(a) : *a;
+    }
+}
+
+constexpr int EPI_BAR = 5;       // the four epilogue warps
+constexpr int EPI_THREADS = 128;
+
+// Epilogue scratch in shared memory.
+struct EpiScratch {
+  float* a;    // [4][MP]
+  float* b;    // [4][MP]
+  float* c;    // [4][MP]
+  int* ia;     // [4][MP] (aliases c for the argmax)
+  int* flag;   // one int
+};
+
+// Turns this tile's 64 output columns (row values yv, already final) into group
+// `grp` of the next phase's prepared activations: per row m, e = 15 - exponent
+// of max|v|, fp16(v * 2^e) in MMA order, the group sum of v * 2^e, 2^-e, and
+// (for a RMSNorm input) the group sum of v^2.  Run by the four epilogue warps.
+template <int BITS, int NT>
+__device__ void prepare_group(const StreamParams& p, const ActBuf& out, int grp, int Kn, int q, int lane,
+                              const float (&yv)[NT][4], bool with_sq, float flag_value, EpiScratch& es) {
+  constexpr int MP = 8 * NT;
+  const int gid = lane >> 2, t = lane & 3;
+  // 1. per column: max |v| and sum v^2 over this warp's 16 rows
+#pragma unroll
+  for (int j = 0; j < NT; ++j)
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      float mx = fmaxf(fabsf(yv[j][c]), fabsf(yv[j][2 + c]));
+      float ss = yv[j][c] * yv[j][c] + yv[j][2 + c] * yv[j][2 + c];
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        ss += __shfl_xor_sync(0xffffffffu, ss, off);
+      }
+      if (gid == 0) {
+        es.a[q * MP + 8 * j + 2 * t + c] = mx;
+        es.b[q * MP + 8 * j + 2 * t + c] = ss;
+      }
+    }
+  named_bar_sync(EPI_BAR, EPI_THREADS);
+  // 2. exponent per column, scaled fp16 values, partial group sums
+  float sc[NT][2], inv[NT][2];
+#pragma unroll
+  for (int j = 0; j < NT; ++j)
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const int m = 8 * j + 2 * t + c;
+      const float mx = fmaxf(fmaxf(es.a[m], es.a[MP + m]), fmaxf(es.a[2 * MP + m], es.a[3 * MP + m]));
+      int e = 0;
+      if (mx > 0.f && mx <= 3.0e38f) {
+        int E;
+        frexpf(mx, &E);
+        e = 15 - E;
+        e = e > 100 ? 100 : (e < -100 ? -100 : e);
+      }
+      sc[j][c] = ldexpf(1.f, e);
+      inv[j][c] = ldexpf(1.f, -e);
+    }
+  const int n_lo = 16 * q + gid, n_hi = n_lo + 8;
+  __half* xp = out.xp;
+#pragma unroll
+  for (int j = 0; j < NT; ++j)
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const int m = 8 * j + 2 * t + c;
+      const float v0 = yv[j][c] * sc[j][c], v1 = yv[j][2 + c] * sc[j][c];
+      xp[((size_t)(2 * grp + (n_lo >> 5)) * MP + m) * 32 + slot_of_phys<BITS>(n_lo & 31)] = __float2half_rn(v0);
+      xp[((size_t)(2 * grp + (n_hi >> 5)) * MP + m) * 32 + slot_of_phys<BITS>(n_hi & 31)] = __float2half_rn(v1);
+      float s = v0 + v1;
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+      if (gid == 0) es.c[q * MP + m] = s;
+    }
+  named_bar_sync(EPI_BAR, EPI_THREADS);
+  // 3. one warp writes the group's sums (fixed quarter order)
+  if (q == 0) {
+    for (int m = lane; m < MP; m += 32) {
+      const float mx = fmaxf(fmaxf(es.a[m], es.a[MP + m]), fmaxf(es.a[2 * MP + m], es.a[3 * MP + m]));
+      int e = 0;
+      if (mx > 0.f && mx <= 3.0e38f) {
+        int E;
+        frexpf(mx, &E);
+        e = 15 - E;
+        e = e > 100 ? 100 : (e < -100 ? -100 : e);
+      }
+      float* xs = out.xs + (size_t)grp * 2 * MP;
+      xs[m] = ((es.c[m] + es.c[MP + m]) + es.c[2 * MP + m]) + es.c[3 * MP + m];
+      xs[MP + m] = ldexpf(1.f, -e);
+      if (with_sq) out.sq[(size_t)grp * MP + m] = ((es.b[m] + es.b[MP + m]) + es.b[2 * MP + m]) + es.b[3 * MP + m];
+      if (grp == 0) out.sq[(size_t)(Kn / GROUP) * MP + m] = flag_value;
+    }
+  }
+  (void)inv;
+  named_bar_sync(EPI_BAR, EPI_THREADS);
+}
+
+// Loads the bf16 values this epilogue thread finishes for 64 output columns
+// starting at `col0` (rows m = 8j + 2t + c, columns col0 + 16q + gid + 8h),
+// zero where m >= M.  Read through L2: the values were written by other CTAs.
+template <int NT>
+__device__ __forceinline__ void load_tile_bf16(float (&v)[NT][4], const __nv_bfloat16* base, int ld, int col0, int M,
+                                               int q, int lane) {
+  const int gid = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int j = 0; j < NT; ++j)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int m = 8 * j + 2 * t + (e & 1);
+      v[j][e] = m < M ? __bfloat162float(__ldcg(base + (size_t)m * ld + col0 + 16 * q + gid + 8 * (e >> 1))) : 0.f;
+    }
+}
+
+// Who finishes what.  Tile `tile` of a phase covers units [tile*upt, (tile+1)*upt);
+// it is finished by the owner of its first unit.  When that CTA's range ends
+// inside the tile, the tile is the last one it works on in the phase, while
+// every other contributor meets the tile first (its range starts inside it):
+// contributors publish early, the finisher reads late.
+__device__ __forceinline__ int tile_finisher(int tile, int upt, int total, int grid) {
+  return unit_owner((long long)tile * upt, total, grid);
+}
+
+// Bounded spin until *ctr >= want (one thread).  Returns false on timeout or abort.
+__device__ __forceinline__ bool wait_counter(const int* ctr, int want, volatile int* abort_v, volatile int* abort_g) {
+  const unsigned long long t0 = global_ns();
+  for (unsigned it = 0;; ++it) {
+    if (*(const volatile int*)ctr >= want) {
+      __threadfence();
+      return true;
+    }
+    if ((it & 15u) == 15u) {
+      if (*abort_v | *abort_g) return false;
+      if (global_ns() - t0 > WAIT_LIMIT_NS) {
+        raise_error(ERR_TIMEOUT_FULL);
+        *abort_v = 1;
+        *abort_g = 1;
+        return false;
+      }
+    }
+    __nanosleep(32);
+  }
+}
+
+// Finishes one tile (all four epilogue warps, each holding 16 rows; values are
+// the full sums, before the RMSNorm row factor).  `pre` holds what was fetched
+// before the tile's sums arrived: the hidden-state rows of a PH_RESID tile or
+// the partner up values of a gate tile whose up half another CTA finished.
+// `g_keep` carries a gate tile's values to its up tile when one CTA finishes
+// both (`pair_here`); otherwise the up tile's finisher publishes its values and
+// the gate tile's finisher, which meets its tile later, combines the two.
+template <int BITS, int NT>
+__device__ void finish_tile(const StreamParams& p, const Phase& ph, int tile, int pair_here, int q, int lane,
+                            float (&tot)[NT][4], const float (&rf)[NT][2], const float (&pre)[NT][4],
+                            float (&g_keep)[NT][4], EpiScratch& es) {
+  constexpr int MP = 8 * NT;
+  const int gid = lane >> 2, t = lane & 3;
+  const int n_lo = tile * BN + 16 * q + gid;  // rows n_lo and n_lo + 8
+  float yv[NT][4];
+#pragma unroll
+  for (int j = 0; j < NT; ++j)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) yv[j][e] = tot[j][e] * rf[j][e & 1];
+
+  if (ph.kind == PH_LOGITS) {
+    // logits and per-row (max, lowest argmax, sum-exp) of these 64 columns
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int m = 8 * j + 2 * t + c;
+        float best = -INFINITY;
+        int bidx = 0x7fffffff;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int n = n_lo + 8 * h;
+          if (n < ph.N) {
+            if (m < p.M) p.logits[(size_t)m * p.ldl + n] = yv[j][2 * h + c];
+            if (yv[j][2 * h + c] > best) { best = yv[j][2 * h + c]; bidx = n; }
+          }
+        }
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          const float ob = __shfl_xor_sync(0xffffffffu, best, off);
+          const int oi = __shfl_xor_sync(0xffffffffu, bidx, off);
+          if (ob > best || (ob == best && oi < bidx)) { best = ob; bidx = oi; }
+        }
+        if (gid == 0) {
+          es.a[q * MP + m] = best;
+          es.ia[q * MP + m] = bidx;
+        }
+      }
+    named_bar_sync(EPI_BAR, EPI_THREADS);
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int m = 8 * j + 2 * t + c;
+        float best = es.a[m];
+        int bidx = es.ia[m];
+#pragma unroll
+        for (int qq = 1; qq < 4; ++qq) {
+          const float ob = es.a[qq * MP + m];
+          const int oi = es.ia[qq * MP + m];
+          if (ob > best || (ob == best && oi < bidx)) { best = ob; bidx = oi; }
+        }
+        float se = 0.f;
+        if (p.inv_temp > 0.f) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            if (n_lo + 8 * h < ph.N) se += expf((yv[j][2 * h + c] - best) * p.inv_temp);
+#pragma unroll
+          for (int off = 4; off < 32; off <<= 1) se += __shfl_xor_sync(0xffffffffu, se, off);
+        }
+        if (gid == 0) es.b[q * MP + m] = se;
+      }
+    named_bar_sync(EPI_BAR, EPI_THREADS);
+    if (q == 0)
+      for (int m = lane; m < MP; m += 32) {
+        float best = es.a[m];
+        int bidx = es.ia[m];
+        for (int qq = 1; qq < 4; ++qq) {
+          const float ob = es.a[qq * MP + m];
+          const int oi = es.ia[qq * MP + m];
+          if (ob > best || (ob == best && oi < bidx)) { best = ob; bidx = oi; }
+        }
+        float* ts = p.tile_stats + ((size_t)tile * MP + m) * 3;
+        ts[0] = best;
+        ts[1] = __int_as_float(bidx);
+        ts[2] = ((es.b[m] + es.b[MP + m]) + es.b[2 * MP + m]) + es.b[3 * MP + m];
+      }
+    named_bar_sync(EPI_BAR, EPI_THREADS);
+    return;
+  }
+
+  if (ph.kind == PH_GATEUP) {
+    // interleaved 64-row blocks: tile 2j = gate rows of block j, tile 2j + 1 = up rows
+    const int blk = tile >> 1, is_up = tile & 1;
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int m = 8 * j + 2 * t + (e & 1);
+        const int col = is_up * ph.half + blk * BN + 16 * q + gid + 8 * (e >> 1);
+        const __nv_bfloat16 v = __float2bfloat16_rn(yv[j][e]);
+        yv[j][e] = m < p.M ? __bfloat162float(v) : 0.f;
+        if (m < p.M) ph.y[(size_t)m * ph.ldy + col] = v;
+      }
+    if (!is_up && pair_here) {  // this CTA finishes the up tile next: keep the gate values
+#pragma unroll
+      for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) g_keep[j][e] = yv[j][e];
+      return;
+    }
+    if (is_up && !pair_here) {  // the gate tile's finisher (another CTA) combines the pair
+      __threadfence();
+      named_bar_sync(EPI_BAR, EPI_THREADS);
+      if (q == 0 && lane == 0) atomicAdd(p.pair_counters + blk, 1);
+      return;
+    }
+    // s = bf16(silu(g) * u)
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int m = 8 * j + 2 * t + (e & 1);
+        const float g = is_up ? g_keep[j][e] : yv[j][e];
+        const float u = is_up ? yv[j][e] : pre[j][e];
+        yv[j][e] = m < p.M ? __bfloat162float(__float2bfloat16_rn(g / (1.f + expf(-g)) * u)) : 0.f;
+      }
+    prepare_group<BITS, NT>(p, p.act[ph.out_buf], blk, ph.half, q, lane, yv, false, -1.f, es);
+    return;
+  }
+
+  if (ph.kind == PH_RESID) {
+    // h = bf16(res + bf16(y)) (res may be y itself); h is the next phase's RMSNorm input
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int m = 8 * j + 2 * t + (e & 1);
+        const int n = n_lo + 8 * (e >> 1);
+        float v = 0.f;
+        if (m < p.M) {
+          const __nv_bfloat16 nb = __float2bfloat16_rn(pre[j][e] + __bfloat162float(__float2bfloat16_rn(yv[j][e])));
+          ph.y[(size_t)m * ph.ldy + n] = nb;
+          v = __bfloat162float(nb);
+        }
+        yv[j][e] = v;
+      }
+    if (ph.out_buf >= 0) prepare_group<BITS, NT>(p, p.act[ph.out_buf], tile, ph.N, q, lane, yv, true, p.rms_eps, es);
+    return;
+  }
+
+  // PH_STORE: bf16 output; the first prep_tiles tiles also feed the next phase
+#pragma unroll
+  for (int j = 0; j < NT; ++j)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int m = 8 * j + 2 * t + (e & 1);
+      const int n = n_lo + 8 * (e >> 1);
+      const __nv_bfloat16 v = __float2bfloat16_rn(yv[j][e]);
+      if (m < p.M && n < ph.N) ph.y[(size_t)m * ph.ldy + n] = v;
+      yv[j][e] = m < p.M ? __bfloat162float(v) : 0.f;
+    }
+  if (tile < ph.prep_tiles)
+    prepare_group<BITS, NT>(p, p.act[ph.out_buf], tile, ph.prep_tiles * BN, q, lane, yv, false, -1.f, es);
+}
+
+// RMSNorm row factors 1/sqrt(mean(x^2) + eps) of the phase input for this
+// thread's columns, or 1 when the input is not an RMSNorm input.  The warp
+// shares the work: LPC lanes per column each sum every LPC-th group of that
+// column, then a fixed shuffle tree adds them.
+template <int NT>
+__device__ __forceinline__ void rms_factors(const ActBuf& a, int K, int lane, float (&rf)[NT][2]) {
+  constexpr int MP = 8 * NT;
+  constexpr int LPC = MP == 8 ? 4 : (MP == 16 ? 2 : 1);  // MP = 24: lanes 24..31 idle
+  const int G = K / GROUP;
+  const float eps = __ldcg(a.sq + (size_t)G * MP);
+  if (!(eps >= 0.f)) {
+#pragma unroll
+    for (int j = 0; j < NT; ++j) rf[j][0] = rf[j][1] = 1.f;
+    return;
+  }
+  const int m = lane % MP, part = lane / MP;
+  float ss = 0.f;
+  if (part < LPC)
+    for (int g = part; g < G; g += LPC) ss += __ldcg(a.sq + (size_t)g * MP + m);
+#pragma unroll
+  for (int off = MP; off < MP * LPC; off <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  const float r_mine = 1.f / sqrtf(ss / (float)K + eps);
+#pragma unroll
+  for (int j = 0; j < NT; ++j)
+#pragma unroll
+    for (int c = 0; c < 2; ++c) rf[j][c] = __shfl_sync(0xffffffffu, r_mine, 8 * j + 2 * (lane & 3) + c);
+}
+
+template <int BITS, int NT>
+__global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_constant__ StreamParams p) {
+  using C = StreamCfg<BITS, NT>;
+  constexpr int S = C::STAGES;
+  constexpr int MP = C::MP;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t full_bar[S], empty_bar[S], res_full[2], res_empty[2];
+  __shared__ int abort_flag;
+  __shared__ int ready_ph;             // highest phase whose grid barrier the producer passed
+  __shared__ int done_ph[MAX_PHASES];  // consumer warps finished with each phase
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float* red = reinterpret_cast<float*>(smem + S * C::STAGE_BYTES);  // result slots [2][4][16*MP]
+  float* epi = red + 2 * 4 * C::RED_FLOATS;
+  EpiScratch es;
+  es.a = epi;
+  es.b = epi + 4 * MP;
+  es.c = epi + 8 * MP;
+  es.ia = reinterpret_cast<int*>(epi + 12 * MP);
+  es.flag = reinterpret_cast<int*>(epi + 16 * MP);
+  volatile int* abort_v = &abort_flag;
+  volatile int* abort_g = p.abort_all;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], NCW);
+    }
+    for (int r = 0; r < 2; ++r) {
+      mbar_init(&res_full[r], 4 * 32);   // the k-half-0 consumer threads
+      mbar_init(&res_empty[r], NEW * 32);  // the epilogue threads
+    }
+    abort_flag = 0;
+    ready_ph = 0;
+    fence_mbar_init();
+  }
+  for (int t = threadIdx.x; t < MAX_PHASES; t += blockDim.x) done_ph[t] = 0;
+  __syncthreads();
+  pdl_trigger();
+
+  if (warp == NCW) {
+    // ================================================================ producer
+    const uint64_t pol_w = l2_evict_first(), pol_x = l2_evict_last();
+    UnitIter iw, ix;  // next unit for weight copies / activation copies
+    iw.start(p, 0);
+    ix = iw;
+    int n_w = 0, n_x = 0;      // units issued so far (weights / activations)
+    int ready = 0;             // highest phase whose activations may be loaded
+    int mapped = -1;           // last phase whose tensor maps were prefetched
+    bool pdl_done = false;
+    unsigned long long t_wait = 0;
+    bool bad = false;
+    auto maps_of = [&](int phase) -> const CUtensorMap* { return p.maps ? p.maps + 3 * phase : p.tm; };
+    auto issue_weights = [&](const UnitIter& it, int i) {
+      if (lane == 0) {
+        const Phase& ph = p.ph[it.phase];
+        const int upt = ph.K / KC, tile = it.u / upt, kc = it.u % upt, s = i % S;
+        uint8_t* st = smem + s * C::STAGE_BYTES;
+        const CUtensorMap* tm = maps_of(it.phase);
+        if (it.phase != mapped) {  // warm the descriptor cache for this phase and the next
+          if (it.phase + 1 < p.n_phases && p.maps)
+            for (int k = 0; k < 3; ++k) prefetch_tensormap(maps_of(it.phase + 1) + k);
+          mapped = it.phase;
+        }
+        mbar_arrive_expect_tx(&full_bar[s], C::TX_BYTES);
+#pragma unroll
+        for (int a = 0; a < C::ATOMS; ++a)
+          tma_load_2d(st + a * (BN * 128), tm, &full_bar[s], kc * C::ROW_BYTES + a * 128, tile * BN, pol_w);
+        tma_load_2d(st + C::S_OFF, tm + 1, &full_bar[s], kc * GPS, tile * BN, pol_w);
+        tma_load_2d(st + C::B_OFF, tm + 2, &full_bar[s], kc * GPS, tile * BN, pol_w);
+      }
+      __syncwarp();
+    };
+    auto issue_acts = [&](const UnitIter& it, int i) {
+      if (lane == 0) {
+        const Phase& ph = p.ph[it.phase];
+        const int kc = it.u % (ph.K / KC), s = i % S;
+        uint8_t* st = smem + s * C::STAGE_BYTES;
+        const ActBuf& a = p.act[ph.in_buf];
+        bulk_load(st + C::X_OFF, a.xp + (size_t)kc * (KC / 32) * MP * 32, C::X_BYTES, &full_bar[s], pol_x);
+        bulk_load(st + C::XS_OFF, a.xs + (size_t)kc * GPS * 2 * MP, C::XS_BYTES, &full_bar[s], pol_x);
+      }
+    };
+    for (;;) {
+      bool progressed = false;
+      // activation copies for units whose phase is ready
+      while (n_x < n_w && ix.phase <= ready && pdl_done) {
+        issue_acts(ix, n_x);
+        ix.next(p);
+        ++n_x;
+        progressed = true;
+      }
+      if (ix.done(p) && n_x == n_w && iw.done(p)) break;
+      // weight copies into the next free stage
+      if (!iw.done(p) && !bad) {
+        bool free_slot = n_w < S;
+        if (!free_slot) {
+          int ok = 0;
+          if (lane == 0) ok = mbar_try_wait(&empty_bar[n_w % S], ((n_w / S) - 1) & 1);
+          free_slot = __shfl_sync(0xffffffffu, ok, 0);
+        }
+        if (free_slot) {
+          issue_weights(iw, n_w);
+          iw.next(p);
+          ++n_w;
+          progressed = true;
+          continue;  // keep the ring full before waiting on anything else
+        }
+      }
+      if (!pdl_done) {  // the first phase's activations come from the previous kernel
+        pdl_wait();
+        pdl_done = true;
+        progressed = true;
+        continue;
+      }
+      // grid barrier for the phase of the oldest unit still waiting for activations:
+      // one counter per transition, so CTAs that skip ahead through phases in
+      // which they have no units cannot stand in for CTAs still working
+      if (n_x < n_w && ix.phase > ready && !bad) {
+        const int need = ix.phase;
+        int go = 0;
+        if (lane == 0 && *(volatile unsigned*)(p.grid_bar + need) >= (unsigned)p.grid) {
+          __threadfence();
+          fence_proxy_async();
+          go = 1;
+        }
+        if (__shfl_sync(0xffffffffu, go, 0)) {
+          ready = need;
+          if (lane == 0) *(volatile int*)&ready_ph = need;
+          progressed = true;
+          continue;
+        }
+      }
+      if (progressed) {
+        t_wait = 0;
+        continue;
+      }
+      // nothing to do: back off briefly, bounded overall
+      __nanosleep(64);
+      const unsigned long long now = global_ns();
+      if (!t_wait) t_wait = now;
+      int stop = (*abort_v | *abort_g) || (now - t_wait > WAIT_LIMIT_NS);
+      stop = __shfl_sync(0xffffffffu, stop, 0);
+      if (stop) {
+        if (lane == 0) {
+          if (!(*abort_v | *abort_g)) raise_error(ERR_TIMEOUT_EMPTY);
+          *abort_v = 1;
+          *abort_g = 1;
+        }
+        bad = true;
+        break;
+      }
+    }
+    // drain copies already issued into the ring before the CTA may exit; after
+    // an abort the stages whose activations were never issued cannot complete,
+    // so give their weight copies a fixed 50 us to land instead
+    if (lane == 0) {
+      if (!bad && !*abort_v) {
+        for (int k = (n_w - S > 0 ? n_w - S : 0); k < n_w; ++k)
+          mbar_wait_bounded(&full_bar[k % S], (k / S) & 1, abort_v);
+      } else {
+        const unsigned long long t0 = global_ns();
+        while (global_ns() - t0 < 50000ull) __nanosleep(1000);
+      }
+    }
+    return;
+  }
+
+  // ================================================================== consumers
+  if (warp < NCW) {
+    const int q = warp >> 1, kh = warp & 1;
+    float tot[NT][4];
+    zero4<NT>(tot);
+    int i = 0, n_te = 0;  // units consumed, tile ends handed over
+    for (int ph_i = 0; ph_i < p.n_phases; ++ph_i) {
+      const Phase& ph = p.ph[ph_i];
+      const int upt = ph.K / KC, total = ph_units(ph);
+      const int u0 = unit_start(blockIdx.x, total, p.grid), u1 = unit_start(blockIdx.x + 1, total, p.grid);
+      for (int u = u0; u < u1; ++u, ++i) {
+        const int kc = u % upt, s = i % S;
+        if (!(*abort_v)) {
+          if (mbar_wait_bounded(&full_bar[s], (i / S) & 1, abort_v)) {
+            consume_stage<BITS, NT>(smem + s * C::STAGE_BYTES, q, kh, lane, tot);
+          } else {
+            raise_error(ERR_TIMEOUT_FULL);
+            *abort_v = 1;
+            *abort_g = 1;
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[s]);
+        if (kc != upt - 1 && u != u1 - 1) continue;
+        // ---- tile end: the two k halves meet in result slot n_te % 2 (fixed
+        // order: half 1 stores, half 0 adds) and the epilogue warps take it
+        const int slot = n_te & 1;
+        if (n_te >= 2 && !(*abort_v) && !mbar_wait_bounded(&res_empty[slot], ((n_te >> 1) - 1) & 1, abort_v)) {
+          raise_error(ERR_TIMEOUT_EMPTY);
+          *abort_v = 1;
+          *abort_g = 1;
+        }
+        float* rb = red + (slot * 4 + q) * C::RED_FLOATS;
+        if (kh == 1) red_store<NT>(rb, tot, lane);
+        named_bar_sync(1 + q, 64);
+        if (kh == 0) {
+          red_add<NT, false>(rb, tot, lane);
+          red_store<NT>(rb, tot, lane);
+          mbar_arrive(&res_full[slot]);
+        }
+        zero4<NT>(tot);
+        ++n_te;
+      }
+    }
+    return;
+  }
+
+  // ================================================================== epilogue
+  // Warps NCW + 1 .. NCW + 4, one per row quarter.  They walk the same tile
+  // ends as the consumers and finish each tile: split-tile fixup, output, the
+  // next phase's prepared input.  Everything a tile's finish needs from other
+  // CTAs (split partials, hidden-state rows, partner up values) is fetched
+  // before the tile's own sums arrive, so the tail of a phase is short.
+  const int q = warp - (NCW + 1);
+  pdl_wait();
+  float rf[NT][2];
+  float g_keep[NT][4];
+  zero4<NT>(g_keep);
+  int n_te = 0;
+  for (int ph_i = 0; ph_i < p.n_phases; ++ph_i) {
+    const Phase& ph = p.ph[ph_i];
+    const int upt = ph.K / KC, total = ph_units(ph);
+    const int u0 = unit_start(blockIdx.x, total, p.grid), u1 = unit_start(blockIdx.x + 1, total, p.grid);
+    if (u0 < u1) {
+      // this phase's inputs are complete once the producer passed its grid barrier
+      if (ph_i > 0) {
+        const unsigned long long t0 = global_ns();
+        while (*(volatile int*)&ready_ph < ph_i) {
+          if ((*abort_v | *abort_g) || global_ns() - t0 > WAIT_LIMIT_NS) break;
+          __nanosleep(32);
+        }
+        __threadfence();
+      }
+      rms_factors<NT>(p.act[ph.in_buf], ph.K, lane, rf);
+      const int first_tile = u0 / upt, last_tile = (u1 - 1) / upt;
+      for (int tile = first_tile; tile <= last_tile; ++tile) {
+        const int fin = tile_finisher(tile, upt, total, p.grid);
+        const int c_last = unit_owner((long long)tile * upt + upt - 1, total, p.grid);
+        const bool finisher = fin == (int)blockIdx.x;
+        float pre[NT][4], part[NT][4];
+        zero4<NT>(pre);
+        zero4<NT>(part);
+        int pair_here = 0;  // gate/up: one CTA finishes both tiles of the block
+        if (finisher) {
+          // ---- fetch ahead: contributors' partials (they met this tile first)
+          if (c_last != fin) {
+            int others = 0;
+            for (int c = fin + 1; c <= c_last; ++c) others += unit_start(c + 1, total, p.grid) > unit_start(c, total, p.grid);
+            int ok = 1;
+            if (q == 0 && lane == 0) ok = wait_counter(p.tile_counters + tile, others, abort_v, abort_g);
+            named_bar_sync(EPI_BAR, EPI_THREADS);
+            for (int c = fin + 1; c <= c_last; ++c)
+              if (unit_start(c + 1, total, p.grid) > unit_start(c, total, p.grid))
+                red_add<NT, true>(p.partials + (((size_t)c * 2) * 4 + q) * C::RED_FLOATS, part, lane);
+            (void)ok;
+          }
+          // ... the hidden-state rows of a residual tile, the partner of a gate tile
+          if (ph.kind == PH_RESID) {
+            load_tile_bf16<NT>(pre, ph.res, ph.ldr, tile * BN, p.M, q, lane);
+          } else if (ph.kind == PH_GATEUP) {
+            const int blk = tile >> 1;
+            pair_here = tile_finisher(2 * blk, upt, total, p.grid) == tile_finisher(2 * blk + 1, upt, total, p.grid);
+            if (!(tile & 1) && !pair_here) {
+              if (q == 0 && lane == 0) wait_counter(p.pair_counters + blk, 1, abort_v, abort_g);
+              named_bar_sync(EPI_BAR, EPI_THREADS);
+              load_tile_bf16<NT>(pre, ph.y, ph.ldy, ph.half + blk * BN, p.M, q, lane);
+              if (q == 0 && lane == 0) p.pair_counters[blk] = 0;
+            }
+          }
+        }
+        // ---- the tile's own sums from the consumers
+        const int slot = n_te & 1;
+        float tot[NT][4];
+        zero4<NT>(tot);
+        const bool ok = !(*abort_v) && mbar_wait_bounded(&res_full[slot], (n_te >> 1) & 1, abort_v);
+        if (ok) {
+          red_add<NT, false>(red + (slot * 4 + q) * C::RED_FLOATS, tot, lane);
+        } else if (!(*abort_v)) {
+          raise_error(ERR_TIMEOUT_FULL);
+          *abort_v = 1;
+          *abort_g = 1;
+        }
+        mbar_arrive(&res_empty[slot]);
+        ++n_te;
+        if (!finisher) {
+          // contributor: publish the partial sums, then count them
+          red_store<NT>(p.partials + (((size_t)blockIdx.x * 2) * 4 + q) * C::RED_FLOATS, tot, lane);
+          __threadfence();
+          named_bar_sync(EPI_BAR, EPI_THREADS);
+          if (q == 0 && lane == 0) atomicAdd(p.tile_counters + tile, 1);
+          continue;
+        }
+        if (c_last != fin) {  // own sums first, then the contributors' in CTA order
+#pragma unroll
+          for (int j = 0; j < NT; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) tot[j][e] += part[j][e];
+          if (q == 0 && lane == 0) p.tile_counters[tile] = 0;
+        }
+        finish_tile<BITS, NT>(p, ph, tile, pair_here, q, lane, tot, rf, pre, g_keep, es);
+      }
+    }
+    // phase done for this warp: publish its global writes, then count it; the
+    // CTA's last epilogue warp to finish the phase arrives on the grid barrier
+    __threadfence();
+    fence_proxy_async();
+    __syncwarp();
+    if (lane == 0 && atomicAdd(&done_ph[ph_i], 1) == NEW - 1 && ph_i + 1 < p.n_phases) {
+      __threadfence();
+      atomicAdd(p.grid_bar + ph_i + 1, 1u);
+    }
+  }
+  named_bar_sync(6, NEW * 32);  // every arrival of this CTA is made
+  // the last CTA to finish resets the grid counters (the workspace's counters
+  // are zero between calls): every CTA has made all its arrivals by then
+  if (q == 0 && lane == 0) {
+    __threadfence();
+    if (atomicAdd(p.exit_counter, 1) == p.grid - 1) {
+      for (int t = 1; t < p.n_phases; ++t) p.grid_bar[t] = 0;
+      *p.exit_counter = 0;
+      __threadfence();
+    }
+  }
+}
+
+}  // namespace sv

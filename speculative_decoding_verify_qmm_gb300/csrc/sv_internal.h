@@ -17,59 +17,93 @@ constexpr int GROUP = 64;        // weights per quantization group (along K)
 constexpr int BN = 64;           // weight rows per CTA tile
 constexpr int KC = 512;          // k per pipeline stage (8 groups)
 constexpr int GPS = KC / GROUP;  // groups per stage
-constexpr int NCW = 8;           // consumer warps per CTA: 2 row halves x 4 k-quarters
-constexpr int QMM_THREADS = (NCW + 1) * 32;
+constexpr int NCW = 8;           // consumer warps per CTA: 4 row quarters x 2 k halves
+constexpr int NEW = 4;           // epilogue warps per CTA: one per row quarter
+constexpr int QMM_THREADS = (NCW + 1 + NEW) * 32;  // consumers, the producer, the epilogue warps
 constexpr int MAX_M = 32;        // rows per verify block handled by the kernels
+constexpr int MAX_PHASES = 272;  // matmuls per launch (64 layers x 4 projections + head, with room)
 
-enum EpiMode : int { EPI_BF16 = 0, EPI_BF16_RESIDUAL = 1, EPI_LOGITS = 2 };
 enum PrepMode : int { PREP_PLAIN = 0, PREP_RMSNORM = 1, PREP_SWIGLU = 2 };
-constexpr size_t COUNTER_BYTES = 262144;  // zero-between-calls counter prefix of every workspace
-constexpr int MAX_TILES = (int)(COUNTER_BYTES / 8);  // two counters (row halves) per tile
+
+// Workspace prefix of counters that are zero between calls.
+constexpr size_t COUNTER_BYTES = 262144;
+constexpr size_t TILE_CTR_OFF = 0;            // per tile of the running phase
+constexpr int MAX_TILES = 32768;
+constexpr size_t PAIR_CTR_OFF = 131072;       // per gate/up block pair
+constexpr size_t GRID_BAR_OFF = 196608;       // grid barrier arrivals, one counter per phase transition
+constexpr size_t EXIT_CTR_OFF = 200704;       // CTAs finished
+constexpr size_t ABORT_OFF = 200708;          // some CTA gave up
+
+// What a phase's finishing epilogue does with its output tile.
+enum PhaseKind : int {
+  PH_STORE = 0,   // y = bf16(out); tiles < prep_tiles also become the next phase's input
+  PH_RESID = 1,   // y (the hidden state) += bf16(out) in place; it becomes the next RMSNorm input
+  PH_GATEUP = 2,  // 64-row gate/up blocks interleaved; silu(gate) * up becomes the next input
+  PH_LOGITS = 3,  // fp32 logits and per-tile row statistics
+};
+
+struct Phase {
+  const uint8_t* wq;
+  const uint16_t* scales;
+  const uint16_t* biases;
+  __nv_bfloat16* y;   // output (PH_RESID: the updated hidden state)
+  const __nv_bfloat16* res;  // PH_RESID: hidden state read (may equal y)
+  int N, K, ldy, ldr;
+  int kind;
+  int prep_tiles;     // PH_STORE: output tiles that feed the next phase
+  int in_buf, out_buf;
+  int half;           // PH_GATEUP: columns per half (gate, then up) of y
+};
+
+// Prepared activations of one phase input (K <= the buffer's capacity).
+struct ActBuf {
+  __half* xp;   // [K/32][MP][32] fp16 x * 2^e, MMA order
+  float* xs;    // [K/64][2][MP]: group sum of x * 2^e, then 2^-e
+  float* sq;    // [K/64 + 1][MP]: group sums of x^2, then eps (RMSNorm input) or -1
+};
+
+struct StreamParams {
+  CUtensorMap tm[3];          // weights, scales, biases of a one-phase launch
+  const CUtensorMap* maps;    // [n_phases][3] in device memory (a round plan), or null: use tm
+  int n_phases, M, MP, grid;
+  float rms_eps;
+  ActBuf act[2];
+  float* partials;        // [grid][2 slots][4 quarters][16*MP]
+  int* tile_counters;
+  int* pair_counters;
+  unsigned* grid_bar;     // [MAX_PHASES]: arrivals for the transition into phase t
+  int* exit_counter;
+  int* abort_all;
+  float* logits; int ldl;
+  float* tile_stats;      // [tiles][MP][3] (max, argmax bits, sum-exp) of the PH_LOGITS phase
+  float inv_temp;
+  Phase ph[MAX_PHASES];
+};
 
 struct PrepArgs {
   const __nv_bfloat16* x; int ldx;      // activations (g for SwiGLU)
   const __nv_bfloat16* x2; int ldx2;    // u for SwiGLU
   const __nv_bfloat16* w; float eps;    // RMSNorm weight (nullable) and epsilon
   int M, MP, K, mode;
-  __half* xp;                           // [K/32][MP][32] fp16 (scaled, MMA order)
-  float* xsum;                          // [K/512][9][MP]: 8 group sums, then 2^-e of the chunk
-  float* rms;                           // [K/512 + 1][MP]: chunk sums of x^2, then eps (or -1: no RMSNorm)
+  ActBuf out;
 };
 
-// Stream-K schedule shared by host and device.  Work unit = (tile, k-chunk):
-// units [c*total/grid, (c+1)*total/grid) belong to CTA c.
-struct Schedule {
-  int N, K, tiles_n, units_per_tile, total_units, grid;
+// Byte offsets of a workspace's pieces: the counter prefix, two activation
+// buffers for inputs up to K_cap wide, the stream-K partials, tile statistics.
+struct Layout {
+  size_t act[2][3], partials, tile_stats, total;
 };
+Layout workspace_layout(int M, int K_cap, int grid, int stat_tiles, int n_act);
+ActBuf act_buf(void* ws, const Layout& L, int a);
+void stream_params_init(StreamParams& p, void* ws, const Layout& L, int M, int grid, float rms_eps);
+int prepare_into(const uint16_t* x, int ldx, int M, int K, int bits, int mode, const uint16_t* x2, int ldx2,
+                 const uint16_t* w, float eps, const ActBuf& out, cudaStream_t s);
 
-struct QmmParams {
-  Schedule sch;
-  int M, MP;                       // rows, rows padded to the n8 MMA tile
-  // prepared activations (written by the prep kernel into the workspace)
-  const __half* xp;                // [K/32][MP][32] fp16, scaled by 2^e per (row, chunk), permuted
-  const float* xsum;               // [K/512][9][MP]: group sums of the scaled rows, then 2^-e
-  const float* rms;                // [K/512 + 1][MP]: RMSNorm partials and eps (eps < 0: none)
-  float* partials;                 // [grid][2 slots][2 halves][32*MP]
-  int* counters;                   // [tiles_n][2], zero between calls
-  // epilogue
-  int mode;
-  __nv_bfloat16* y; int ldy;       // EPI_BF16 / EPI_BF16_RESIDUAL
-  const __nv_bfloat16* res; int ldres;
-  float* logits; int ldl;          // EPI_LOGITS
-  float* tile_stats;               // [tiles_n*2][MP][3] per 32-row half (max, argmax bits, sumexp)
-  float inv_temp;                  // 1/T, 0 for greedy
-};
-
-// Byte offsets of the pieces of a qmm workspace.  The counters always sit in
-// the fixed prefix; the prepared activations depend only on (M, K), so a
-// prepare call and the run calls that consume it agree on where they are.
-struct QmmWorkspace {
-  size_t counters, xp, xsum, rms, partials, tile_stats, total;
-};
-
-Schedule make_schedule(int N, int K, int grid_limit);
-QmmWorkspace qmm_workspace_layout(int M, int N, int K, int grid, bool with_stats);
 int device_sm_count();
+// Tensor maps of one quantized weight: codes in 128-byte swizzled boxes of
+// 64 rows, scales and biases in 8-group x 64-row boxes.
+int encode_weight_maps(CUtensorMap (&out)[3], const void* wq, const void* scales, const void* biases, int N, int K,
+                       int bits);
 int fail(int status, const char* fmt, ...);
 int check_weight(const uint32_t* wq, const uint16_t* scales, const uint16_t* biases, int N, int K, int bits,
                  int group, int M);
@@ -77,10 +111,11 @@ int cuda_fail(cudaError_t e, const char* what);
 size_t align256(size_t v);
 bool aligned(const void* p, size_t a);
 size_t prepare_bytes(int M, int K);
-size_t qmm_bytes(int M, int N, int K, bool stats);
+size_t qmm_bytes(int M, int N, int K, int bits, bool stats);
 size_t accept_bytes(int B, int rows);
 int qmm_prepare_internal(const uint16_t* x, int ldx, int M, int K, int bits, int mode, const uint16_t* x2, int ldx2,
                          const uint16_t* w, float eps, void* ws, cudaStream_t s);
+// mode: 0 = store bf16, 1 = add to the residual, 2 = logits with row statistics
 int qmm_run_internal(const uint32_t* wq, const uint16_t* scales, const uint16_t* biases, int N, int K, int bits,
                      int M, int mode, uint16_t* y, int ldy, const uint16_t* residual, int ldr, float* logits,
                      int ldl, float temperature, float* row_max, float* row_sumexp, int32_t* row_argmax, void* ws,
@@ -96,8 +131,9 @@ cudaError_t read_and_clear_error_word(unsigned int* out);
 
 // Launchers (return cudaError_t of the launch).
 cudaError_t launch_prep(const PrepArgs& a, int bits, int mode, cudaStream_t s);
-cudaError_t launch_qmm(int bits, int NT, const CUtensorMap& tw, const CUtensorMap& ts, const CUtensorMap& tb,
-                       const QmmParams& p, cudaStream_t s);
+// cooperative when the launch has more than one phase (grid barriers)
+cudaError_t launch_stream(int bits, const StreamParams& p, cudaStream_t s);
+int stream_max_grid(int bits, int MP);
 cudaError_t launch_lmhead_finalize(const float* tile_stats, int tiles_n, int MP, int M, float inv_temp,
                                    float* row_max, float* row_sumexp, int32_t* row_argmax, cudaStream_t s);
 

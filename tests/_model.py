@@ -40,9 +40,22 @@ def to_device(w):
             "K": w["K"], "bits": w["bits"]}
 
 
+def interleave_gate_up(gate, up, block=64):
+    """gate | up rows interleaved in blocks of 64 (the round's gate_up layout)."""
+    I = gate["wq"].shape[0]
+
+    def inter(a, b):
+        a = np.asarray(a).reshape(I // block, block, -1)
+        b = np.asarray(b).reshape(I // block, block, -1)
+        return np.ascontiguousarray(np.stack([a, b], axis=1).reshape(2 * I, -1))
+    return {"wq": inter(gate["wq"], up["wq"]), "scales": inter(gate["scales"], up["scales"]),
+            "biases": inter(gate["biases"], up["biases"]), "K": gate["K"], "bits": gate["bits"]}
+
+
 def device_layers(layers):
     return [{"qkv": to_device(_stack([l["q"], l["k"], l["v"]])), "o": to_device(l["o"]),
-             "gate_up": to_device(_stack([l["gate"], l["up"]])), "down": to_device(l["down"])} for l in layers]
+             "gate_up": to_device(interleave_gate_up(l["gate"], l["up"])), "down": to_device(l["down"])}
+            for l in layers]
 
 
 def device_random_model(seed, n_layers, hidden, q_dim, kv_dim, inter, vocab, bits, stats):
@@ -68,9 +81,11 @@ def host_copy(w, rows=None):
             "biases": w["biases"][sl].cpu().numpy().view(np.uint16), "K": w["K"], "bits": w["bits"]}
 
 
-def split_device_layer(dl, q_dim, kv_dim, inter):
-    """Host per-projection dicts of one stacked device layer."""
+def split_device_layer(dl, q_dim, kv_dim, inter, block=64):
+    """Host per-projection dicts of one stacked device layer (gate/up de-interleaved)."""
+    gu = host_copy(dl["gate_up"])
+    blk = (np.arange(2 * inter) // block) % 2
+    pick = lambda sel: {k: (v[blk == sel] if k in ("wq", "scales", "biases") else v) for k, v in gu.items()}
     return {"q": host_copy(dl["qkv"], (0, q_dim)), "k": host_copy(dl["qkv"], (q_dim, q_dim + kv_dim)),
             "v": host_copy(dl["qkv"], (q_dim + kv_dim, q_dim + 2 * kv_dim)), "o": host_copy(dl["o"]),
-            "gate": host_copy(dl["gate_up"], (0, inter)), "up": host_copy(dl["gate_up"], (inter, 2 * inter)),
-            "down": host_copy(dl["down"])}
+            "gate": pick(0), "up": pick(1), "down": host_copy(dl["down"])}

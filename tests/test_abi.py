@@ -95,3 +95,18 @@ def test_bf16_ulp_helper():
     bits = quant.f32_to_bf16_bits(np.abs(x))
     nxt = quant.bf16_bits_to_f32((bits + 1).astype(np.uint16)).astype(np.float64)
     assert np.allclose(nxt - quant.bf16_bits_to_f32(bits), bf16_ulp(x), rtol=0, atol=0)
+
+
+def test_round_plan_argument_errors_on_host(raw):
+    """The plan calls reject bad models and buffers before touching the device."""
+    assert raw.sv_round_plan_bytes(None) == 0
+    assert raw.sv_round_plan_init(None, P(256), 1 << 20) == binding.SV_EINVAL
+    layers = (binding.Layer * 1)()
+    model = binding.Model(0, 1024, 1024, 2048, 1000, 8, 1e-6, layers, binding.QWeight())
+    assert raw.sv_round_plan_bytes(ctypes.byref(model)) == 0              # no layers
+    assert raw.sv_round_plan_init(ctypes.byref(model), P(256), 1 << 20) == binding.SV_EINVAL
+    model.n_layers = 68                                                     # more than 4 * 67 + 1 phases
+    assert raw.sv_round_plan_bytes(ctypes.byref(model)) == 0
+    model.n_layers = 1
+    assert raw.sv_round_plan_bytes(ctypes.byref(model)) == 5 * 3 * 128     # 5 projections x 3 descriptors
+    assert raw.sv_round_plan_init(ctypes.byref(model), P(256), 1 << 20) == binding.SV_EINVAL  # null weights

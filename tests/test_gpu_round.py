@@ -114,6 +114,20 @@ def test_batched_round_four_requests(lib):
         assert (int(n[b]), toks[offs[b]:offs[b] + n[b]].tolist()) == tuple(want[b])
 
 
+def test_round_refuses_a_plan_built_for_another_model(lib):
+    layers, head = _model.host_model(1450, 1, bits=4, stats=synthetic.TINY_4BIT, **TINY)
+    dl, dh = _model.device_layers(layers), _model.to_device(head)
+    a = lib.make_model(dl, dh, TINY["hidden"], TINY["q_dim"], TINY["inter"], TINY["vocab"], 4)
+    dh2 = _model.to_device(head)                     # same values, other device pointers
+    b = lib.make_model(dl, dh2, TINY["hidden"], TINY["q_dim"], TINY["inter"], TINY["vocab"], 4)
+    b.plan = a.plan
+    h0 = dev_bf16(synthetic.activations(synthetic.rng(1451), 1, TINY["hidden"]))
+    with pytest.raises(Exception, match="plan"):
+        _round(lib, b, [0, 1], h0, 0.0, draft=torch.zeros(1, dtype=torch.int32, device="cuda"))
+    _round(lib, a, [0, 1], h0, 0.0, draft=torch.zeros(1, dtype=torch.int32, device="cuda"))
+    assert lib.device_error() == 0
+
+
 QWEN8B = dict(hidden=4096, q_dim=4096, kv_dim=1024, inter=12288, vocab=151936)
 
 
