@@ -73,6 +73,7 @@ int sv_qmm_verify_noalloc(const uint32_t* wq, const uint16_t* scales, const uint
   // left them set).  No allocation: a memset of the array itself.
   const size_t counter_bytes = (size_t)((N + BN - 1) / BN) * 4;
   cudaError_t e = cudaMemsetAsync(ws, 0, counter_bytes, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(static_cast<uint8_t*>(ws) + EXIT_CTR_OFF, 0, 8, s);  // exit, abort
   if (e != cudaSuccess) return cuda_fail(e, "clear scratch counters");
   st = qmm_prepare_internal(x, ldx, M, K, bits, PREP_PLAIN, nullptr, 0, nullptr, 0.f, ws, s);
   if (st) return st;

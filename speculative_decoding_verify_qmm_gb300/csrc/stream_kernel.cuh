@@ -385,14 +385,12 @@ __device__ __forceinline__ int tile_finisher(int tile, int upt, int total, int g
   return unit_owner((long long)tile * upt, total, grid);
 }
 
-// Bounded spin until *ctr >= want (one thread).  Returns false on timeout or abort.
+// Bounded spin (one thread) until *ctr >= want, with acquire semantics.
+// Returns false on timeout or abort.
 __device__ __forceinline__ bool wait_counter(const int* ctr, int want, volatile int* abort_v, volatile int* abort_g) {
   const unsigned long long t0 = global_ns();
   for (unsigned it = 0;; ++it) {
-    if (*(const volatile int*)ctr >= want) {
-      __threadfence();
-      return true;
-    }
+    if ((int)ld_acquire(reinterpret_cast<const unsigned*>(ctr)) >= want) return true;
     if ((it & 15u) == 15u) {
       if (*abort_v | *abort_g) return false;
       if (global_ns() - t0 > WAIT_LIMIT_NS) {
@@ -402,7 +400,6 @@ __device__ __forceinline__ bool wait_counter(const int* ctr, int want, volatile 
         return false;
       }
     }
-    __nanosleep(32);
   }
 }
 
@@ -518,9 +515,8 @@ __device__ void finish_tile(const StreamParams& p, const Phase& ph, int tile, in
       return;
     }
     if (is_up && !pair_here) {  // the gate tile's finisher (another CTA) combines the pair
-      __threadfence();
       named_bar_sync(EPI_BAR, EPI_THREADS);
-      if (q == 0 && lane == 0) atomicAdd(p.pair_counters + blk, 1);
+      if (q == 0 && lane == 0) red_release_add(reinterpret_cast<unsigned*>(p.pair_counters + blk), 1u);
       return;
     }
     // s = bf16(silu(g) * u)
@@ -609,7 +605,6 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
   __shared__ uint64_t full_bar[S], empty_bar[S], res_full[2], res_empty[2];
   __shared__ int abort_flag;
   __shared__ int ready_ph;             // highest phase whose grid barrier the producer passed
-  __shared__ int done_ph[MAX_PHASES];  // consumer warps finished with each phase
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* red = reinterpret_cast<float*>(smem + S * C::STAGE_BYTES);  // result slots [2][4][16*MP]
   float* epi = red + 2 * 4 * C::RED_FLOATS;
@@ -636,7 +631,6 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
     ready_ph = 0;
     fence_mbar_init();
   }
-  for (int t = threadIdx.x; t < MAX_PHASES; t += blockDim.x) done_ph[t] = 0;
   __syncthreads();
   pdl_trigger();
 
@@ -698,7 +692,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
         bool free_slot = n_w < S;
         if (!free_slot) {
           int ok = 0;
-          if (lane == 0) ok = mbar_try_wait(&empty_bar[n_w % S], ((n_w / S) - 1) & 1);
+          if (lane == 0) ok = mbar_test_wait(&empty_bar[n_w % S], ((n_w / S) - 1) & 1);
           free_slot = __shfl_sync(0xffffffffu, ok, 0);
         }
         if (free_slot) {
@@ -721,14 +715,13 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
       if (n_x < n_w && ix.phase > ready && !bad) {
         const int need = ix.phase;
         int go = 0;
-        if (lane == 0 && *(volatile unsigned*)(p.grid_bar + need) >= (unsigned)p.grid) {
-          __threadfence();
+        if (lane == 0 && ld_acquire(p.grid_bar + need) >= (unsigned)p.grid) {
           fence_proxy_async();
           go = 1;
         }
         if (__shfl_sync(0xffffffffu, go, 0)) {
           ready = need;
-          if (lane == 0) *(volatile int*)&ready_ph = need;
+          if (lane == 0) st_release_cta(&ready_ph, need);
           progressed = true;
           continue;
         }
@@ -835,11 +828,10 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
       // this phase's inputs are complete once the producer passed its grid barrier
       if (ph_i > 0) {
         const unsigned long long t0 = global_ns();
-        while (*(volatile int*)&ready_ph < ph_i) {
+        while (ld_acquire_cta(&ready_ph) < ph_i) {
           if ((*abort_v | *abort_g) || global_ns() - t0 > WAIT_LIMIT_NS) break;
           __nanosleep(32);
         }
-        __threadfence();
       }
       rms_factors<NT>(p.act[ph.in_buf], ph.K, lane, rf);
       const int first_tile = u0 / upt, last_tile = (u1 - 1) / upt;
@@ -895,9 +887,8 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
         if (!finisher) {
           // contributor: publish the partial sums, then count them
           red_store<NT>(p.partials + (((size_t)blockIdx.x * 2) * 4 + q) * C::RED_FLOATS, tot, lane);
-          __threadfence();
           named_bar_sync(EPI_BAR, EPI_THREADS);
-          if (q == 0 && lane == 0) atomicAdd(p.tile_counters + tile, 1);
+          if (q == 0 && lane == 0) red_release_add(reinterpret_cast<unsigned*>(p.tile_counters + tile), 1u);
           continue;
         }
         if (c_last != fin) {  // own sums first, then the contributors' in CTA order
@@ -910,15 +901,12 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
         finish_tile<BITS, NT>(p, ph, tile, pair_here, q, lane, tot, rf, pre, g_keep, es);
       }
     }
-    // phase done for this warp: publish its global writes, then count it; the
-    // CTA's last epilogue warp to finish the phase arrives on the grid barrier
-    __threadfence();
+    // phase done: the epilogue warps' writes (which other CTAs read through
+    // the generic proxy and through bulk copies) are published by one release
+    // after a barrier over the four warps
     fence_proxy_async();
-    __syncwarp();
-    if (lane == 0 && atomicAdd(&done_ph[ph_i], 1) == NEW - 1 && ph_i + 1 < p.n_phases) {
-      __threadfence();
-      atomicAdd(p.grid_bar + ph_i + 1, 1u);
-    }
+    named_bar_sync(EPI_BAR, EPI_THREADS);
+    if (q == 0 && lane == 0 && ph_i + 1 < p.n_phases) red_release_add(p.grid_bar + ph_i + 1, 1u);
   }
   named_bar_sync(6, NEW * 32);  // every arrival of this CTA is made
   // the last CTA to finish resets the grid counters (the workspace's counters
