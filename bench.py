@@ -286,6 +286,25 @@ def cpu_cores():
     return os.cpu_count()
 
 
+# -------------------------------------------------------- ncu DRAM traffic
+# DRAM bytes (read + write) per launch of the persistent kernel, from one ncu
+# capture of a smaller round (profiles/stream_kernel_m8_4layers.md), scaled to
+# a full launch by weight bytes; valid only for the kernel source it was taken
+# on, so the source's hash is checked and the figure dropped when it differs.
+TRAFFIC_CAPTURE = {"sha256": "a44cfc2017c86a58cbb4db558370fb9cb46a58123b6a5f7a6e25cd1f593f8bef", "M": 8,
+                   "bytes": 1485691000 + 8433408, "weight_bytes": 1481211904}
+
+
+def measured_traffic(M, wbytes):
+    import hashlib
+    if not TRAFFIC_CAPTURE or TRAFFIC_CAPTURE["M"] != M:
+        return None
+    src = os.path.join(ROOT, "speculative_decoding_verify_qmm_gb300", "csrc", "stream_kernel.cuh")
+    if hashlib.sha256(open(src, "rb").read()).hexdigest() != TRAFFIC_CAPTURE["sha256"]:
+        return None
+    return round(TRAFFIC_CAPTURE["bytes"] * wbytes / TRAFFIC_CAPTURE["weight_bytes"])
+
+
 # --------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -294,17 +313,21 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=SHAPE["n_layers"],
+                    help="fewer layers of the same shapes: a small case for profiler captures, not a bench line")
+    ap.add_argument("--only-m", type=int, default=0, help="time only this row count (default: 1, 8 and 16)")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
+    shape = dict(SHAPE, n_layers=args.layers)
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
-    M = 8
-    wbytes = weight_bytes(SHAPE)
-    config = {"workload": "Qwen3-8B-shaped verify round: 36 layers x (q|k|v, o, gate|up, down) 8-bit g64 + "
-                          "lm_head 4096->151936 + spec_accept",
+    M = args.only_m or 8
+    wbytes = weight_bytes(shape)
+    config = {"workload": "Qwen3-8B-shaped verify round: %d layers x (q|k|v, o, gate|up, down) 8-bit g64 + "
+                          "lm_head 4096->151936 + spec_accept" % shape["n_layers"],
               "M": M, "m": M - 1, "temperature": TEMPERATURE, "draft_agreement": 0.7,
-              "weight_bytes_per_round": wbytes, "l2": "no flush: 8.04 GB of weights per round >> 129 MB L2",
+              "weight_bytes_per_round": wbytes, "l2": "no flush: %.2f GB of weights per round >> 129 MB L2" % (wbytes / 1e9),
               "parallelism": "replicas" if args.gpus > 1 else "single GPU"}
 
     if args.impl == "reference":
@@ -340,20 +363,22 @@ def main():
     import synthetic
     lib = binding.load()
 
-    layers, head = _model.device_random_model(1234 + rank, SHAPE["n_layers"], SHAPE["hidden"], SHAPE["q_dim"],
-                                              SHAPE["kv_dim"], SHAPE["inter"], SHAPE["vocab"], SHAPE["bits"],
+    layers, head = _model.device_random_model(1234 + rank, shape["n_layers"], shape["hidden"], shape["q_dim"],
+                                              shape["kv_dim"], shape["inter"], shape["vocab"], shape["bits"],
                                               synthetic.LARGE_8BIT)
+    ms = (M,) if args.only_m else (1, 8, 16)
     rounds = {}
-    for Mx in (1, 8, 16):
-        rnd = Round(lib, layers, head, SHAPE, Mx, seed=77 + Mx)
+    for Mx in ms:
+        rnd = Round(lib, layers, head, shape, Mx, seed=77 + Mx)
         rnd.capture()
         rounds[Mx] = rnd
 
     with ClockSampler(local) as clk:
         t = {}
-        for Mx in (1, 16):
-            t[Mx] = time_rounds(rounds[Mx], args.steps, args.warmup, dist)
-        t[8] = time_rounds(rounds[8], args.steps, args.warmup, dist)
+        for Mx in ms:
+            if Mx != M:
+                t[Mx] = time_rounds(rounds[Mx], args.steps, args.warmup, dist)
+        t[M] = time_rounds(rounds[M], args.steps, args.warmup, dist)
     clocks = clk.summary()
     err = lib.device_error()
     if err:
@@ -372,36 +397,40 @@ def main():
     gbs = {k: wbytes / (v * 1e-6) / 1e9 for k, v in us.items()}
 
     # dominant kernel: the persistent matmul launch of the round
-    dur_s = matmul_kernel_roofline(rounds[8], max(10, args.steps // 2))
+    dur_s = matmul_kernel_roofline(rounds[M], max(10, args.steps // 2))
     achieved = wbytes / dur_s / 1e9
-    e2e_us, h2d, d2h = e2e_rounds(lib, rounds[8], max(10, args.steps // 2))
+    e2e_us, h2d, d2h = e2e_rounds(lib, rounds[M], max(10, args.steps // 2))
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        est, secs, sample = oracle_round_sample(SHAPE, M)
+        est, secs, sample = oracle_round_sample(shape, M)
         cpu = {"value": est, "unit": "us/round", "cores": cpu_cores(), "kind": "oracle", "sample": sample,
                "cpu_seconds": secs}
 
+    traffic = measured_traffic(M, wbytes)
     launches_per_round = 4  # input preparation, the projections, row-statistics merge, accept
     line = {
-        "metric": METRIC, "value": us[8] / world, "unit": "us/round", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": us[8] / 1e3, "higher_is_better": False, "scaling": "weak",
+        "metric": METRIC, "value": us[M] / world, "unit": "us/round", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": us[M] / 1e3, "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "q8 codes x bf16 activations (fp16 MMA), fp32 accumulate",
         "data": "synthetic (seeded random weights and activations of the stated shapes)", "config": config,
         "us_per_round": {str(k): round(v, 2) for k, v in sorted(us.items())},
         "weight_stream_gbs": {str(k): round(v, 1) for k, v in sorted(gbs.items())},
         "pct_of_measured_hbm": {str(k): round(100 * v / hbm, 1) for k, v in sorted(gbs.items())},
         "pct_of_8tbs": {str(k): round(100 * v / NOMINAL_HBM_GBS, 1) for k, v in sorted(gbs.items())},
-        "cost_ratio_vs_M1": {str(k): round(us[k] / us[1], 3) for k in sorted(us)},
+        "cost_ratio_vs_M1": {str(k): round(us[k] / us[1], 3) for k in sorted(us)} if 1 in us else None,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                     "frac": round(achieved / hbm, 3), "traffic": None,
-                     "kernel": "stream_kernel<8,1>: all 145 projections of the M=8 round in one launch",
+                     "frac": round(achieved / hbm, 3), "traffic": traffic,
+                     "traffic_unit": "bytes per launch (ncu dram read + write, scaled from the profiled case)",
+                     "kernel": "stream_kernel<8,%d>: all %d projections of the M=%d round in one launch" % (
+                         (M + 7) // 8, 4 * shape["n_layers"] + 1, M),
                      "us_per_launch": round(dur_s * 1e6, 1), "bytes_per_launch": round(wbytes),
-                     "peak_source": "MEASURED_PEAKS.json hbm_gbs" if peaks else "fallback 6.8 TB/s"},
+                     "peak_source": "MEASURED_PEAKS.json hbm_gbs (burst copy), of measured" if peaks
+                     else "fallback 6.8 TB/s"},
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_us, 2), "unit": "us/round", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_round * args.steps,
-        "gpu_launches_note": "kernels per timed M=8 region (%d per round)" % launches_per_round,
+        "gpu_launches_note": "kernels per timed M=%d region (%d per round)" % (M, launches_per_round),
         "clocks": clocks,
     }
     if rank == 0:
