@@ -13,8 +13,9 @@
 //     Y[m, n] += scale[n,g] * sum_{k in g} X[m,k] * (code[n,k] - off)  +  (bias[n,g] + off*scale[n,g]) * sum_{k in g} X[m,k]
 //
 // with the inner sums on the tensor cores (codes are exact small integers in
-// fp16, `off` = 128 or 8 centres them) and the two group terms in fp32, so no
-// weight is ever rounded to a 16-bit float.  Activations arrive as fp16 scaled
+// fp16: 8-bit codes enter as 1024 + c, off = -1024, straight from one byte
+// permute; 4-bit codes are centred, off = 8) and the two group terms in fp32,
+// so no weight is ever rounded to a 16-bit float.  Activations arrive as fp16 scaled
 // by 2^e per (row, group) so that every bf16 value keeps all its bits.
 //
 // Work and data flow (one CTA per SM, stream-K over (64-row tile, 512-k chunk)
@@ -112,12 +113,10 @@ struct UnitIter {
 };
 
 // ---------------------------------------------------------- code conversion
-// fp16 pair (1024 + c0, 1024 + c1) from two code bytes, then centred: (c0 - 128, c1 - 128).
-__device__ __forceinline__ uint32_t cvt8(uint32_t codes, uint32_t sel) {
-  uint32_t v = __byte_perm(codes, 0x64646464u, sel);
-  __half2 h = __hadd2(*reinterpret_cast<__half2*>(&v), __half2half2(__ushort_as_half(0xE480)));  // -1152
-  return *reinterpret_cast<uint32_t*>(&h);
-}
+// fp16 pair (1024 + c0, 1024 + c1) from two code bytes: one byte permute
+// against the exponent byte 0x64 (1024 is exact, and so is 1024 + c for any
+// byte c).  The 1024 is taken back out in fp32 with the group's bias term.
+__device__ __forceinline__ uint32_t cvt8(uint32_t codes, uint32_t sel) { return __byte_perm(codes, 0x64646464u, sel); }
 // Four fp16 pairs (n - 8) from the eight 4-bit codes of one word; nibble j is element 8t + j.
 // P0 = (n0, n4), P1 = (n1, n5), P2 = (n2, n6), P3 = (n3, n7).
 __device__ __forceinline__ void cvt4(uint32_t w, uint32_t (&P)[4]) {
@@ -162,7 +161,8 @@ template <int BITS, int NT>
 __device__ __forceinline__ void consume_stage(const uint8_t* st, int q, int kh, int lane, float (&tot)[NT][4]) {
   using C = StreamCfg<BITS, NT>;
   constexpr int MP = C::MP;
-  constexpr float OFF = BITS == 8 ? 128.f : 8.f;
+  // the tensor cores see code - OFF: 8-bit codes as 1024 + c, 4-bit ones centred as n - 8
+  constexpr float OFF = BITS == 8 ? -1024.f : 8.f;
   const int gid = lane >> 2, t = lane & 3;
   const uint32_t w_base = smem_u32(st);
   const uint32_t x_base = smem_u32(st + C::X_OFF);
