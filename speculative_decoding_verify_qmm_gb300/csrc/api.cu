@@ -135,11 +135,27 @@ static int encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base,
   return SV_OK;
 }
 
+// Codes as a 3D view (byte within a 128-byte piece, row, piece) so that one
+// copy brings all pieces of a stage: shared memory receives [piece][row][128 B]
+// with the 128-byte swizzle, the layout the consumers read.
+static int encode_codes(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t N, uint32_t pieces) {
+  auto fn = encode_fn();
+  if (!fn) return fail(SV_ECUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t dims[3] = {128, N, row_bytes / 128};
+  const cuuint64_t strides[2] = {row_bytes, 128};
+  const cuuint32_t box[3] = {128, (cuuint32_t)BN, pieces};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(SV_ECUDA, "cuTensorMapEncodeTiled (codes) failed (CUresult %d)", (int)r);
+  return SV_OK;
+}
+
 int encode_weight_maps(CUtensorMap (&out)[3], const void* wq, const void* scales, const void* biases, int N, int K,
                        int bits) {
   const uint64_t row_bytes = (uint64_t)K * bits / 8, G = (uint64_t)(K / GROUP);
-  int st = encode_2d(&out[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, row_bytes, (uint64_t)N, row_bytes, 128, BN,
-                     CU_TENSOR_MAP_SWIZZLE_128B);
+  int st = encode_codes(&out[0], wq, row_bytes, (uint64_t)N, (uint32_t)(KC * bits / 8 / 128));
   if (st) return st;
   st = encode_2d(&out[1], CU_TENSOR_MAP_DATA_TYPE_UINT16, scales, G, (uint64_t)N, G * 2, GPS, BN,
                  CU_TENSOR_MAP_SWIZZLE_NONE);

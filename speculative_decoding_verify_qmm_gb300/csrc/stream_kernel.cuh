@@ -21,10 +21,11 @@
 // Work and data flow (one CTA per SM, stream-K over (64-row tile, 512-k chunk)
 // units of every phase, so every SM streams the same number of weight bytes):
 //   * warp 8 (producer) fills a ring of shared-memory stages with TMA copies:
-//     the tile's codes as 64-row x 128-byte boxes with the 128-byte swizzle
-//     (ldmatrix then reads them without bank conflicts), one 64 x 8 box each
-//     of scales and biases, and the matching slice of the prepared
-//     activations as plain bulk copies.  It runs ahead into the next phase's
+//     the tile's codes as one 3D box of 128-byte pieces x 64 rows with the
+//     128-byte swizzle (ldmatrix then reads them without bank conflicts),
+//     one 64 x 8 box each of scales and biases, and the matching slice of
+//     the prepared activations as plain bulk copies (a lane completes only a
+//     few copy instructions per microsecond, so a stage takes five).  It runs ahead into the next phase's
 //     weights while the current phase drains; only the activation copies wait
 //     for the grid-wide phase barrier.
 //   * warps 0-7 (consumers) are 4 row quarters x 2 k halves: ldmatrix the codes,
@@ -659,9 +660,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
           mapped = it.phase;
         }
         mbar_arrive_expect_tx(&full_bar[s], C::TX_BYTES);
-#pragma unroll
-        for (int a = 0; a < C::ATOMS; ++a)
-          tma_load_2d(st + a * (BN * 128), tm, &full_bar[s], kc * C::ROW_BYTES + a * 128, tile * BN, pol_w);
+        tma_load_3d(st, tm, &full_bar[s], 0, tile * BN, kc * C::ATOMS, pol_w);  // all pieces of the stage
         tma_load_2d(st + C::S_OFF, tm + 1, &full_bar[s], kc * GPS, tile * BN, pol_w);
         tma_load_2d(st + C::B_OFF, tm + 2, &full_bar[s], kc * GPS, tile * BN, pol_w);
       }
@@ -730,11 +729,14 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
         t_wait = 0;
         continue;
       }
-      // nothing to do: back off briefly, bounded overall
-      __nanosleep(64);
+      // nothing to do: back off briefly, bounded overall.  The abort flags are
+      // looked at only once a wait has lasted 20 us, so an idle turn costs no
+      // global-memory round trip.
+      __nanosleep(32);
       const unsigned long long now = global_ns();
       if (!t_wait) t_wait = now;
-      int stop = (*abort_v | *abort_g) || (now - t_wait > WAIT_LIMIT_NS);
+      int stop = 0;
+      if (now - t_wait > 20000ull && lane == 0) stop = (*abort_v | *abort_g) || (now - t_wait > WAIT_LIMIT_NS);
       stop = __shfl_sync(0xffffffffu, stop, 0);
       if (stop) {
         if (lane == 0) {
