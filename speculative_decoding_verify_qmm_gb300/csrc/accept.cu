@@ -11,7 +11,10 @@
 // the (at most 31) accept decisions of its request from fp64 ratios, then sums
 // the draw weights of its chunk in fp64.  The last CTA of a request to finish
 // (atomic counter, no spinning) turns the chunk sums into a prefix, finds the
-// chunk holding u[m] * Z and scans it in index order.
+// chunk holding u[m] * Z, and the one thread whose sub-range of that chunk
+// holds the crossing scans it in index order.  Sums and prefixes are shuffle
+// trees in a fixed order: fp64 is slow on this part, and serial fp64 chains
+// dominated the step's time.
 #include "sv_internal.h"
 #include "sv_ptx.cuh"
 #include "sv_kernels.h"
@@ -19,6 +22,34 @@
 namespace sv {
 
 constexpr int ACC_THREADS = 256;
+constexpr int ACC_CACHE = 8192;  // vocabulary chunk held in shared memory by the drawing CTA
+
+// Warp reductions and scans in a fixed order (shuffle trees), so every run
+// adds the same values in the same order.
+__device__ __forceinline__ double warp_sum(double v) {
+#pragma unroll
+  for (int off = 16; off; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
+__device__ __forceinline__ double warp_incl_scan(double v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const double o = __shfl_up_sync(0xffffffffu, v, off);
+    if (lane >= off) v += o;
+  }
+  return v;
+}
+__device__ __forceinline__ int warp_min(int v) {
+#pragma unroll
+  for (int off = 16; off; off >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, off));
+  return v;
+}
+__device__ __forceinline__ int warp_max(int v) {
+#pragma unroll
+  for (int off = 16; off; off >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, off));
+  return v;
+}
 
 __global__ void __launch_bounds__(ACC_THREADS) accept_kernel(const AcceptParams p) {
   pdl_trigger();
@@ -42,8 +73,9 @@ __global__ void __launch_bounds__(ACC_THREADS) accept_kernel(const AcceptParams 
 
   __shared__ int s_j, s_last, s_cstar, s_flag;
   __shared__ double s_pre, s_theta;
-  __shared__ double s_w[ACC_THREADS], s_p[ACC_THREADS];
-  __shared__ int s_i[ACC_THREADS];
+  __shared__ double s_w[ACC_THREADS / 32], s_p[ACC_THREADS / 32];
+  __shared__ int s_i[2 * (ACC_THREADS / 32)];
+  __shared__ float s_cache[ACC_CACHE];
 
   // ---- accept decisions (fp64 ratio, one lane per draft)
   if (tid < 32) {
@@ -54,12 +86,17 @@ __global__ void __launch_bounds__(ACC_THREADS) accept_kernel(const AcceptParams 
         rej = true;
         if (chunk == 0) raise_error(ERR_BAD_INPUT);
       } else {
-        const double qd = p.q[(size_t)(qd0 + tid) * p.ldq + d];
-        const double z = p.logits[(size_t)(r0 + tid) * p.ldl + d];
-        const double pd = exp((z - (double)p.row_max[r0 + tid]) / (double)p.temperature) /
-                          (double)p.row_sumexp[r0 + tid];
-        const double r = qd == 0.0 ? INFINITY : pd / qd;
-        rej = !((double)p.u[r0 + tid] < r);
+        // fp32 ratio (relative error a few 1e-7); fp64 only when u is near it
+        const float qd = p.q[(size_t)(qd0 + tid) * p.ldq + d];
+        const float z = p.logits[(size_t)(r0 + tid) * p.ldl + d];
+        const float zmx = p.row_max[r0 + tid], se = p.row_sumexp[r0 + tid], ui = p.u[r0 + tid];
+        const float r32 = qd == 0.f ? INFINITY : expf((z - zmx) / p.temperature) / se / qd;
+        if (fabsf(ui - r32) > 1e-5f * fmaxf(1.f, r32)) {
+          rej = !(ui < r32);
+        } else {
+          const double pd = exp(((double)z - (double)zmx) / (double)p.temperature) / (double)se;
+          rej = !((double)ui < pd / (double)qd);
+        }
       }
     }
     const unsigned mask = __ballot_sync(0xffffffffu, rej);
@@ -80,24 +117,36 @@ __global__ void __launch_bounds__(ACC_THREADS) accept_kernel(const AcceptParams 
   // ---- chunk sums of the draw weights (and of p, for the zero-residual fallback)
   const int NB = p.nb;
   const int k0 = (int)((long long)chunk * V / NB), k1 = (int)((long long)(chunk + 1) * V / NB);
-  double sw = 0.0, sp = 0.0;
-  for (int k = k0 + tid; k < k1; k += ACC_THREADS) {
-    float pk;
-    const float wk = weight(k, pk);
-    sw += wk;
-    sp += pk;
+  float sw = 0.f, sp = 0.f;  // at most a few dozen terms per thread: fp32 holds them to ~1e-7
+  // four elements per turn with their loads issued together (the loop is
+  // latency-bound: every element is a load from L2)
+  for (int k = k0 + tid; k < k1; k += 4 * ACC_THREADS) {
+    float wk[4], pk[4];
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const int kk = k + v * ACC_THREADS;
+      wk[v] = pk[v] = 0.f;
+      if (kk < k1) wk[v] = weight(kk, pk[v]);
+    }
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      sw += wk[v];
+      sp += pk[v];
+    }
   }
-  s_w[tid] = sw;
-  s_p[tid] = sp;
+  const int lane = tid & 31, wid = tid >> 5;
+  const double dsw = warp_sum((double)sw), dsp = warp_sum((double)sp);
+  if (lane == 0) {
+    s_w[wid] = dsw;
+    s_p[wid] = dsp;
+  }
   __syncthreads();
-  for (int w = ACC_THREADS / 2; w; w >>= 1) {
-    if (tid < w) { s_w[tid] += s_w[tid + w]; s_p[tid] += s_p[tid + w]; }
-    __syncthreads();
-  }
   if (tid == 0) {
+    double tw = 0.0, tp = 0.0;
+    for (int w = 0; w < ACC_THREADS / 32; ++w) { tw += s_w[w]; tp += s_p[w]; }  // fixed order
     double* cs = p.chunk_sums + ((size_t)b * NB + chunk) * 2;
-    cs[0] = s_w[0];
-    cs[1] = s_p[0];
+    cs[0] = tw;
+    cs[1] = tp;
     __threadfence();
     s_last = atomicAdd(p.counters + b, 1) == NB - 1;
   }
@@ -105,39 +154,40 @@ __global__ void __launch_bounds__(ACC_THREADS) accept_kernel(const AcceptParams 
   if (!s_last) return;
   __threadfence();
 
-  // ---- last CTA of the request: locate u[m] * Z
-  __shared__ double s_cw[64], s_cp[64];
-  if (tid < NB) {
-    const double* cs = p.chunk_sums + ((size_t)b * NB + tid) * 2;
-    s_cw[tid] = __ldcg(cs);
-    s_cp[tid] = __ldcg(cs + 1);
-  }
-  __syncthreads();
-  if (tid == 0) {
-    double zw = 0.0, zp = 0.0;
-    for (int c = 0; c < NB; ++c) { zw += s_cw[c]; zp += s_cp[c]; }
+  // ---- last CTA of the request: locate u[m] * Z among the chunks (warp 0:
+  // lane l holds chunks l and l + 32; inclusive scans by shuffles)
+  if (wid == 0) {
+    const double* cs = p.chunk_sums + (size_t)b * NB * 2;
+    double w0 = lane < NB ? __ldcg(cs + 2 * lane) : 0.0, w1 = lane + 32 < NB ? __ldcg(cs + 2 * (lane + 32)) : 0.0;
+    double p0 = lane < NB ? __ldcg(cs + 2 * lane + 1) : 0.0, p1 = lane + 32 < NB ? __ldcg(cs + 2 * (lane + 32) + 1) : 0.0;
+    const double zw = warp_sum(w0) + warp_sum(w1), zp = warp_sum(p0) + warp_sum(p1);
     const int use_p = resid && !(zw > 0.0);
-    const double* sums = use_p ? s_cp : s_cw;
+    double a0 = use_p ? p0 : w0, a1 = use_p ? p1 : w1;
     const double Z = use_p ? zp : zw;
     const double theta = (double)p.u[r0 + m] * Z;
-    double pre = 0.0;
-    int cstar = -1;
-    for (int c = 0; c < NB; ++c) {
-      if (pre + sums[c] > theta) { cstar = c; break; }
-      pre += sums[c];
-    }
+    const double i0 = warp_incl_scan(a0);
+    const double i1 = warp_incl_scan(a1) + __shfl_sync(0xffffffffu, i0, 31);
+    // first chunk whose inclusive prefix exceeds theta
+    const unsigned c0m = __ballot_sync(0xffffffffu, lane < NB && i0 > theta);
+    const unsigned c1m = __ballot_sync(0xffffffffu, lane + 32 < NB && i1 > theta);
+    int cstar = c0m ? __ffs(c0m) - 1 : (c1m ? 32 + __ffs(c1m) - 1 : -1);
     int flag = use_p;  // bit 0: draw from p; bit 1: take the last positive weight
     if (cstar < 0) {   // rounding left theta at the total: last chunk with positive weight
       flag |= 2;
-      for (int c = NB - 1; c >= 0; --c)
-        if (sums[c] > 0.0) { cstar = c; break; }
-      if (cstar < 0) cstar = NB - 1;
+      const unsigned q0 = __ballot_sync(0xffffffffu, lane < NB && a0 > 0.0);
+      const unsigned q1 = __ballot_sync(0xffffffffu, lane + 32 < NB && a1 > 0.0);
+      cstar = q1 ? 63 - __clz(q1) : (q0 ? 31 - __clz(q0) : NB - 1);
     }
-    s_cstar = cstar;
-    s_pre = pre;
-    s_theta = theta;
-    s_flag = flag;
-    p.counters[b] = 0;
+    // exclusive prefix of chunk cstar
+    const double excl0 = i0 - a0, excl1 = i1 - a1;
+    const double pre = cstar < 32 ? __shfl_sync(0xffffffffu, excl0, cstar & 31) : __shfl_sync(0xffffffffu, excl1, cstar & 31);
+    if (lane == 0) {
+      s_cstar = cstar;
+      s_pre = pre;
+      s_theta = theta;
+      s_flag = flag;
+      p.counters[b] = 0;
+    }
   }
   __syncthreads();
   const int cstar = s_cstar, flag = s_flag;
@@ -145,50 +195,77 @@ __global__ void __launch_bounds__(ACC_THREADS) accept_kernel(const AcceptParams 
   const int c0 = (int)((long long)cstar * V / NB), c1 = (int)((long long)(cstar + 1) * V / NB);
   const int len = c1 - c0, per = (len + ACC_THREADS - 1) / ACC_THREADS;
   const int a = c0 + tid * per, e = min(c1, a + per);
-  double local = 0.0;
-  int last_pos = -1;
-  for (int k = a; k < e; ++k) {
+  // the chunk's draw weights, filled with coalesced loads when they fit in
+  // shared memory; each thread then sums its contiguous sub-range
+  const bool cached = len <= ACC_CACHE;
+  if (cached) {
+    for (int k = c0 + tid; k < c1; k += 4 * ACC_THREADS) {
+      float wv[4];
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const int kk = k + v * ACC_THREADS;
+        float pk = 0.f, wk = 0.f;
+        if (kk < c1) wk = weight(kk, pk);
+        wv[v] = from_p ? pk : wk;
+      }
+#pragma unroll
+      for (int v = 0; v < 4; ++v)
+        if (k + v * ACC_THREADS < c1) s_cache[k + v * ACC_THREADS - c0] = wv[v];
+    }
+    __syncthreads();
+  }
+  auto draw_weight = [&](int k) -> float {
+    if (cached) return s_cache[k - c0];
     float pk;
     const float wk = weight(k, pk);
-    const float wv = from_p ? pk : wk;
-    local += wv;
+    return from_p ? pk : wk;
+  };
+  float local32 = 0.f;
+  int last_pos = -1;
+  for (int k = a; k < e; ++k) {
+    const float wv = draw_weight(k);
+    local32 += wv;
     if (wv > 0.f) last_pos = k;
   }
-  s_w[tid] = local;
+  const double local = local32;
+  const double incl = warp_incl_scan(local);
+  if (lane == 31) s_w[wid] = incl;
   __syncthreads();
-  if (tid == 0) {  // exclusive prefix over the threads' sub-ranges, in index order
-    double run = s_pre;
-    for (int i = 0; i < ACC_THREADS; ++i) { const double v = s_w[i]; s_w[i] = run; run += v; }
+  if (wid == 0) {
+    const double t = lane < ACC_THREADS / 32 ? s_w[lane] : 0.0;
+    const double ti = warp_incl_scan(t);
+    if (lane < ACC_THREADS / 32) s_p[lane] = ti - t;  // exclusive prefix of each warp
   }
   __syncthreads();
+  const double start = s_pre + s_p[wid] + (incl - local);
+  // only the thread whose sub-range holds the crossing scans it
   int cand = 0x7fffffff;
-  if (!(flag & 2)) {
-    double run = s_w[tid];
+  if (!(flag & 2) && start <= s_theta && start + local > s_theta) {
+    double run = start;
     for (int k = a; k < e; ++k) {
-      float pk;
-      const float wk = weight(k, pk);
-      run += from_p ? pk : wk;
+      run += draw_weight(k);
       if (run > s_theta) { cand = k; break; }
     }
+    if (cand == 0x7fffffff) cand = last_pos >= 0 ? last_pos : e - 1;  // rounding inside the range
   }
-  s_i[tid] = cand;
+  cand = warp_min(cand);
+  if (lane == 0) s_i[wid] = cand;
+  const int lp = warp_max(last_pos);
   __syncthreads();
-  for (int w = ACC_THREADS / 2; w; w >>= 1) {
-    if (tid < w) s_i[tid] = min(s_i[tid], s_i[tid + w]);
-    __syncthreads();
-  }
-  int token = s_i[0];
-  __syncthreads();
-  if (token == 0x7fffffff) {  // no crossing inside the chunk: last positive weight
-    s_i[tid] = last_pos;
-    __syncthreads();
-    for (int w = ACC_THREADS / 2; w; w >>= 1) {
-      if (tid < w) s_i[tid] = max(s_i[tid], s_i[tid + w]);
-      __syncthreads();
-    }
-    token = s_i[0] < 0 ? c1 - 1 : s_i[0];
-  }
   if (tid == 0) {
+    int token = 0x7fffffff;
+    for (int w = 0; w < ACC_THREADS / 32; ++w) token = min(token, s_i[w]);
+    s_j = token;
+  }
+  if (lane == 0) s_i[ACC_THREADS / 32 + wid] = lp;
+  __syncthreads();
+  if (tid == 0) {
+    int token = s_j;
+    if (token == 0x7fffffff) {  // no crossing inside the chunk: last positive weight
+      int lastp = -1;
+      for (int w = 0; w < ACC_THREADS / 32; ++w) lastp = max(lastp, s_i[ACC_THREADS / 32 + w]);
+      token = lastp < 0 ? c1 - 1 : lastp;
+    }
     for (int i = 0; i < j; ++i) p.out_tokens[r0 + i] = p.draft[qd0 + i];
     p.out_tokens[r0 + j] = token;
     p.out_len[b] = j + 1;
