@@ -18,16 +18,19 @@
 // so no weight is ever rounded to a 16-bit float.  Activations arrive as fp16 scaled
 // by 2^e per (row, group) so that every bf16 value keeps all its bits.
 //
-// Work and data flow (one CTA per SM, stream-K over (64-row tile, 512-k chunk)
-// units of every phase, so every SM streams the same number of weight bytes):
-//   * warp 8 (producer) fills a ring of shared-memory stages with TMA copies:
-//     the tile's codes as one 3D box of 128-byte pieces x 64 rows with the
-//     128-byte swizzle (ldmatrix then reads them without bank conflicts),
-//     one 64 x 8 box each of scales and biases, and the matching slice of
-//     the prepared activations as plain bulk copies (a lane completes only a
-//     few copy instructions per microsecond, so a stage takes five).  It runs ahead into the next phase's
-//     weights while the current phase drains; only the activation copies wait
-//     for the grid-wide phase barrier.
+// Work and data flow (one CTA per SM; stream-K over (64-row tile, 512-k chunk)
+// units, so every SM streams the same number of weight bytes, except that
+// short phases of at most one tile per CTA give each CTA one whole tile):
+//   * warps 8 and 13 (producers) fill a ring of shared-memory stages with TMA
+//     copies, warp 8 the weights and warp 13 the activations (a lane
+//     completes only a few copy instructions per microsecond, so the copies
+//     are few, large, and split over two warps): the tile's codes as one 3D
+//     box of 128-byte pieces x 64 rows with the 128-byte swizzle (ldmatrix
+//     then reads them without bank conflicts), one 64 x 8 box each of scales
+//     and biases, and the matching slice of the prepared activations as plain
+//     bulk copies.  The weights run ahead into the next phase while the
+//     current phase drains; only the activation copies wait for the
+//     grid-wide phase barrier.
 //   * warps 0-7 (consumers) are 4 row quarters x 2 k halves: ldmatrix the codes,
 //     turn them into fp16 with byte-permute / LOP3, mma.sync m16n8k16 against
 //     the activation fragments, fold each group into fp32 sums.  At a tile's
@@ -65,7 +68,6 @@ struct StreamCfg {
   static constexpr int XS_OFF = X_OFF + X_BYTES;
   static constexpr int S_OFF = (XS_OFF + XS_BYTES + 127) / 128 * 128;
   static constexpr int B_OFF = S_OFF + SB_BYTES;
-  static constexpr int TX_BYTES = W_BYTES + X_BYTES + XS_BYTES + 2 * SB_BYTES;  // full boxes, ragged tiles too
   static constexpr int STAGE_BYTES = (B_OFF + SB_BYTES + 1023) / 1024 * 1024;  // swizzle atoms 1024-aligned
   static constexpr int RED_FLOATS = 16 * MP;        // one quarter's 16 rows
   static constexpr int RED_BYTES = 2 * 4 * RED_FLOATS * 4;  // result slot x quarter
@@ -82,9 +84,13 @@ struct StreamCfg {
 
 // ------------------------------------------------------------ schedule math
 __device__ __forceinline__ int ph_units(const Phase& ph) { return ((ph.N + BN - 1) / BN) * (ph.K / KC); }
+// Units of a phase are split over `grid` CTAs in contiguous ranges (stream-K),
+// or, for a phase flagged whole-tile, one tile per CTA (grid = tiles; CTAs
+// beyond it get nothing), so that no tile is split.
 __device__ __forceinline__ int unit_start(int c, int total, int grid) {
-  return static_cast<int>(static_cast<long long>(c) * total / grid);
+  return c >= grid ? total : static_cast<int>(static_cast<long long>(c) * total / grid);
 }
+__device__ __forceinline__ int phase_grid(const Phase& ph, int grid) { return ph.whole ? (ph.N + BN - 1) / BN : grid; }
 __device__ __forceinline__ int unit_owner(long long u, int total, int grid) {
   return static_cast<int>(((u + 1) * grid - 1) / total);
 }
@@ -103,8 +109,9 @@ struct UnitIter {
       ++phase;
       if (phase >= p.n_phases) return;
       total = ph_units(p.ph[phase]);
-      u = unit_start(blockIdx.x, total, p.grid);
-      u_end = unit_start(blockIdx.x + 1, total, p.grid);
+      const int g = phase_grid(p.ph[phase], p.grid);
+      u = unit_start(blockIdx.x, total, g);
+      u_end = unit_start(blockIdx.x + 1, total, g);
     } while (u >= u_end);
   }
   __device__ __forceinline__ bool done(const StreamParams& p) const { return phase >= p.n_phases; }
@@ -621,7 +628,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full_bar[s], 1);
+      mbar_init(&full_bar[s], 2);  // the weight warp and the activation warp
       mbar_init(&empty_bar[s], NCW);
     }
     for (int r = 0; r < 2; ++r) {
@@ -635,97 +642,85 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
   __syncthreads();
   pdl_trigger();
 
-  if (warp == NCW) {
-    // ================================================================ producer
+  if (warp == NCW || warp == XPW) {
+    // ============================================================ producers
+    // Warp NCW copies each stage's weights (codes, scales, biases); warp XPW
+    // copies its activations once the stage's phase is open.  Two issuing
+    // warps: one lane completes only a few copy instructions per
+    // microsecond.  Each arrives once per stage use on the stage's full
+    // barrier (count 2) with its own byte count.
+    const bool is_x = warp == XPW;
     const uint64_t pol_w = l2_evict_first(), pol_x = l2_evict_last();
-    UnitIter iw, ix;  // next unit for weight copies / activation copies
-    iw.start(p, 0);
-    ix = iw;
-    int n_w = 0, n_x = 0;      // units issued so far (weights / activations)
-    int ready = 0;             // highest phase whose activations may be loaded
-    int mapped = -1;           // last phase whose tensor maps were prefetched
-    bool pdl_done = false;
+    UnitIter it;
+    it.start(p, 0);
+    int n = 0;                 // units issued so far by this warp
+    int ready = 0;             // (activation warp) highest phase whose activations may be loaded
+    int mapped = -1;           // (weight warp) last phase whose tensor maps were prefetched
+    bool pdl_done = !is_x;     // the weight warp never reads what the previous kernel wrote
     unsigned long long t_wait = 0;
     bool bad = false;
     auto maps_of = [&](int phase) -> const CUtensorMap* { return p.maps ? p.maps + 3 * phase : p.tm; };
-    auto issue_weights = [&](const UnitIter& it, int i) {
-      if (lane == 0) {
-        const Phase& ph = p.ph[it.phase];
-        const int upt = ph.K / KC, tile = it.u / upt, kc = it.u % upt, s = i % S;
-        uint8_t* st = smem + s * C::STAGE_BYTES;
-        const CUtensorMap* tm = maps_of(it.phase);
-        if (it.phase != mapped) {  // warm the descriptor cache for this phase and the next
-          if (it.phase + 1 < p.n_phases && p.maps)
-            for (int k = 0; k < 3; ++k) prefetch_tensormap(maps_of(it.phase + 1) + k);
-          mapped = it.phase;
-        }
-        mbar_arrive_expect_tx(&full_bar[s], C::TX_BYTES);
-        tma_load_3d(st, tm, &full_bar[s], 0, tile * BN, kc * C::ATOMS, pol_w);  // all pieces of the stage
-        tma_load_2d(st + C::S_OFF, tm + 1, &full_bar[s], kc * GPS, tile * BN, pol_w);
-        tma_load_2d(st + C::B_OFF, tm + 2, &full_bar[s], kc * GPS, tile * BN, pol_w);
+    while (!it.done(p)) {
+      bool go = false;
+      // the stage must be free: its previous unit consumed
+      bool free_slot = n < S;
+      if (!free_slot) {
+        int ok = 0;
+        if (lane == 0) ok = mbar_test_wait(&empty_bar[n % S], ((n / S) - 1) & 1);
+        free_slot = __shfl_sync(0xffffffffu, ok, 0);
       }
-      __syncwarp();
-    };
-    auto issue_acts = [&](const UnitIter& it, int i) {
-      if (lane == 0) {
-        const Phase& ph = p.ph[it.phase];
-        const int kc = it.u % (ph.K / KC), s = i % S;
-        uint8_t* st = smem + s * C::STAGE_BYTES;
-        const ActBuf& a = p.act[ph.in_buf];
-        bulk_load(st + C::X_OFF, a.xp + (size_t)kc * (KC / 32) * MP * 32, C::X_BYTES, &full_bar[s], pol_x);
-        bulk_load(st + C::XS_OFF, a.xs + (size_t)kc * GPS * 2 * MP, C::XS_BYTES, &full_bar[s], pol_x);
-      }
-    };
-    for (;;) {
-      bool progressed = false;
-      // activation copies for units whose phase is ready
-      while (n_x < n_w && ix.phase <= ready && pdl_done) {
-        issue_acts(ix, n_x);
-        ix.next(p);
-        ++n_x;
-        progressed = true;
-      }
-      if (ix.done(p) && n_x == n_w && iw.done(p)) break;
-      // weight copies into the next free stage
-      if (!iw.done(p) && !bad) {
-        bool free_slot = n_w < S;
-        if (!free_slot) {
-          int ok = 0;
-          if (lane == 0) ok = mbar_test_wait(&empty_bar[n_w % S], ((n_w / S) - 1) & 1);
-          free_slot = __shfl_sync(0xffffffffu, ok, 0);
-        }
-        if (free_slot) {
-          issue_weights(iw, n_w);
-          iw.next(p);
-          ++n_w;
-          progressed = true;
-          continue;  // keep the ring full before waiting on anything else
-        }
-      }
-      if (!pdl_done) {  // the first phase's activations come from the previous kernel
-        pdl_wait();
-        pdl_done = true;
-        progressed = true;
-        continue;
-      }
-      // grid barrier for the phase of the oldest unit still waiting for activations:
-      // one counter per transition, so CTAs that skip ahead through phases in
-      // which they have no units cannot stand in for CTAs still working
-      if (n_x < n_w && ix.phase > ready && !bad) {
-        const int need = ix.phase;
-        int go = 0;
-        if (lane == 0 && ld_acquire(p.grid_bar + need) >= (unsigned)p.grid) {
-          fence_proxy_async();
-          go = 1;
-        }
-        if (__shfl_sync(0xffffffffu, go, 0)) {
-          ready = need;
-          if (lane == 0) st_release_cta(&ready_ph, need);
-          progressed = true;
+      if (free_slot) {
+        if (!is_x) {
+          go = true;
+        } else if (!pdl_done) {  // the first phase's activations come from the previous kernel
+          pdl_wait();
+          pdl_done = true;
           continue;
+        } else if (it.phase <= ready) {
+          go = true;
+        } else {
+          // grid barrier of this unit's phase: one counter per transition, so
+          // CTAs that skip ahead through phases in which they have no units
+          // cannot stand in for CTAs still working
+          int pass = 0;
+          if (lane == 0 && ld_acquire(p.grid_bar + it.phase) >= (unsigned)p.grid) {
+            fence_proxy_async();
+            pass = 1;
+          }
+          if (__shfl_sync(0xffffffffu, pass, 0)) {
+            ready = it.phase;
+            if (lane == 0) st_release_cta(&ready_ph, ready);
+            go = true;
+          }
         }
       }
-      if (progressed) {
+      if (go) {
+        if (lane == 0) {
+          const Phase& ph = p.ph[it.phase];
+          const int upt = ph.K / KC, kc = it.u % upt, sg = n % S;
+          uint8_t* st = smem + sg * C::STAGE_BYTES;
+          if (!is_x) {
+            const int tile = it.u / upt;
+            const CUtensorMap* tm = maps_of(it.phase);
+            if (it.phase != mapped) {  // warm the descriptor cache for this phase and the next
+              if (it.phase + 1 < p.n_phases && p.maps)
+                for (int k = 0; k < 3; ++k) prefetch_tensormap(maps_of(it.phase + 1) + k);
+              mapped = it.phase;
+            }
+            mbar_arrive_expect_tx(&full_bar[sg], C::W_BYTES + 2 * C::SB_BYTES);
+            tma_load_3d(st, tm, &full_bar[sg], 0, tile * BN, kc * C::ATOMS, pol_w);  // all pieces of the stage
+            tma_load_2d(st + C::S_OFF, tm + 1, &full_bar[sg], kc * GPS, tile * BN, pol_w);
+            tma_load_2d(st + C::B_OFF, tm + 2, &full_bar[sg], kc * GPS, tile * BN, pol_w);
+          } else {
+            const ActBuf& a = p.act[ph.in_buf];
+            mbar_arrive_expect_tx(&full_bar[sg], C::X_BYTES + C::XS_BYTES);
+            bulk_load(st + C::X_OFF, a.xp + (size_t)kc * (KC / 32) * MP * 32, C::X_BYTES, &full_bar[sg], pol_x);
+            bulk_load(st + C::XS_OFF, a.xs + (size_t)kc * GPS * 2 * MP, C::XS_BYTES, &full_bar[sg], pol_x);
+          }
+        }
+        __syncwarp();
+        it.next(p);
+        ++n;
         t_wait = 0;
         continue;
       }
@@ -749,11 +744,11 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
       }
     }
     // drain copies already issued into the ring before the CTA may exit; after
-    // an abort the stages whose activations were never issued cannot complete,
-    // so give their weight copies a fixed 50 us to land instead
+    // an abort a stage may never complete, so give its copies a fixed 50 us
+    // to land instead
     if (lane == 0) {
       if (!bad && !*abort_v) {
-        for (int k = (n_w - S > 0 ? n_w - S : 0); k < n_w; ++k)
+        for (int k = (n - S > 0 ? n - S : 0); k < n; ++k)
           mbar_wait_bounded(&full_bar[k % S], (k / S) & 1, abort_v);
       } else {
         const unsigned long long t0 = global_ns();
@@ -772,7 +767,8 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
     for (int ph_i = 0; ph_i < p.n_phases; ++ph_i) {
       const Phase& ph = p.ph[ph_i];
       const int upt = ph.K / KC, total = ph_units(ph);
-      const int u0 = unit_start(blockIdx.x, total, p.grid), u1 = unit_start(blockIdx.x + 1, total, p.grid);
+      const int pg = phase_grid(ph, p.grid);
+      const int u0 = unit_start(blockIdx.x, total, pg), u1 = unit_start(blockIdx.x + 1, total, pg);
       for (int u = u0; u < u1; ++u, ++i) {
         const int kc = u % upt, s = i % S;
         if (!(*abort_v)) {
@@ -825,7 +821,8 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
   for (int ph_i = 0; ph_i < p.n_phases; ++ph_i) {
     const Phase& ph = p.ph[ph_i];
     const int upt = ph.K / KC, total = ph_units(ph);
-    const int u0 = unit_start(blockIdx.x, total, p.grid), u1 = unit_start(blockIdx.x + 1, total, p.grid);
+    const int pg = phase_grid(ph, p.grid);
+    const int u0 = unit_start(blockIdx.x, total, pg), u1 = unit_start(blockIdx.x + 1, total, pg);
     if (u0 < u1) {
       // this phase's inputs are complete once the producer passed its grid barrier
       if (ph_i > 0) {
@@ -838,8 +835,8 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
       rms_factors<NT>(p.act[ph.in_buf], ph.K, lane, rf);
       const int first_tile = u0 / upt, last_tile = (u1 - 1) / upt;
       for (int tile = first_tile; tile <= last_tile; ++tile) {
-        const int fin = tile_finisher(tile, upt, total, p.grid);
-        const int c_last = unit_owner((long long)tile * upt + upt - 1, total, p.grid);
+        const int fin = tile_finisher(tile, upt, total, pg);
+        const int c_last = unit_owner((long long)tile * upt + upt - 1, total, pg);
         const bool finisher = fin == (int)blockIdx.x;
         float pre[NT][4], part[NT][4];
         zero4<NT>(pre);
@@ -849,12 +846,12 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
           // ---- fetch ahead: contributors' partials (they met this tile first)
           if (c_last != fin) {
             int others = 0;
-            for (int c = fin + 1; c <= c_last; ++c) others += unit_start(c + 1, total, p.grid) > unit_start(c, total, p.grid);
+            for (int c = fin + 1; c <= c_last; ++c) others += unit_start(c + 1, total, pg) > unit_start(c, total, pg);
             int ok = 1;
             if (q == 0 && lane == 0) ok = wait_counter(p.tile_counters + tile, others, abort_v, abort_g);
             named_bar_sync(EPI_BAR, EPI_THREADS);
             for (int c = fin + 1; c <= c_last; ++c)
-              if (unit_start(c + 1, total, p.grid) > unit_start(c, total, p.grid))
+              if (unit_start(c + 1, total, pg) > unit_start(c, total, pg))
                 red_add<NT, true>(p.partials + (((size_t)c * 2) * 4 + q) * C::RED_FLOATS, part, lane);
             (void)ok;
           }
@@ -863,7 +860,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
             load_tile_bf16<NT>(pre, ph.res, ph.ldr, tile * BN, p.M, q, lane);
           } else if (ph.kind == PH_GATEUP) {
             const int blk = tile >> 1;
-            pair_here = tile_finisher(2 * blk, upt, total, p.grid) == tile_finisher(2 * blk + 1, upt, total, p.grid);
+            pair_here = tile_finisher(2 * blk, upt, total, pg) == tile_finisher(2 * blk + 1, upt, total, pg);
             if (!(tile & 1) && !pair_here) {
               if (q == 0 && lane == 0) wait_counter(p.pair_counters + blk, 1, abort_v, abort_g);
               named_bar_sync(EPI_BAR, EPI_THREADS);

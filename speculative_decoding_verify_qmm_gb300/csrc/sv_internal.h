@@ -19,7 +19,8 @@ constexpr int KC = 512;          // k per pipeline stage (8 groups)
 constexpr int GPS = KC / GROUP;  // groups per stage
 constexpr int NCW = 8;           // consumer warps per CTA: 4 row quarters x 2 k halves
 constexpr int NEW = 4;           // epilogue warps per CTA: one per row quarter
-constexpr int QMM_THREADS = (NCW + 1 + NEW) * 32;  // consumers, the producer, the epilogue warps
+constexpr int XPW = NCW + 1 + NEW;  // the activation-copy warp
+constexpr int QMM_THREADS = (NCW + 1 + NEW + 1) * 32;  // consumers, weight producer, epilogue warps, activation producer
 constexpr int MAX_M = 32;        // rows per verify block handled by the kernels
 constexpr int MAX_PHASES = 272;  // matmuls per launch (64 layers x 4 projections + head, with room)
 
@@ -53,6 +54,7 @@ struct Phase {
   int prep_tiles;     // PH_STORE: output tiles that feed the next phase
   int in_buf, out_buf;
   int half;           // PH_GATEUP: columns per half (gate, then up) of y
+  int whole;          // one whole tile per CTA instead of stream-K (tiles <= grid)
 };
 
 // Prepared activations of one phase input (K <= the buffer's capacity).
