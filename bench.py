@@ -315,6 +315,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=SHAPE["n_layers"],
                     help="fewer layers of the same shapes: a small case for profiler captures, not a bench line")
+    ap.add_argument("--layout", default="packed", choices=["packed", "canonical"],
+                    help="weights streamed from the unit-packed copy (sv_qmm_pack) or the canonical tensors")
     ap.add_argument("--only-m", type=int, default=0, help="time only this row count (default: 1, 8 and 16)")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
@@ -328,7 +330,7 @@ def main():
                           "lm_head 4096->151936 + spec_accept" % shape["n_layers"],
               "M": M, "m": M - 1, "temperature": TEMPERATURE, "draft_agreement": 0.7,
               "weight_bytes_per_round": wbytes, "l2": "no flush: %.2f GB of weights per round >> 129 MB L2" % (wbytes / 1e9),
-              "parallelism": "replicas" if args.gpus > 1 else "single GPU"}
+              "weight_layout": args.layout, "parallelism": "replicas" if args.gpus > 1 else "single GPU"}
 
     if args.impl == "reference":
         if rank != 0:
@@ -366,6 +368,10 @@ def main():
     layers, head = _model.device_random_model(1234 + rank, shape["n_layers"], shape["hidden"], shape["q_dim"],
                                               shape["kv_dim"], shape["inter"], shape["vocab"], shape["bits"],
                                               synthetic.LARGE_8BIT)
+    if args.layout == "packed":      # one-time re-layout at load time, outside every timed region
+        for w in [w for layer in layers for w in layer.values()] + [head]:
+            w["packed"] = lib.pack(w)
+        torch.cuda.synchronize()
     ms = (M,) if args.only_m else (1, 8, 16)
     rounds = {}
     for Mx in ms:

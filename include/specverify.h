@@ -251,6 +251,7 @@ typedef struct {
   const uint16_t* scales;
   const uint16_t* biases;
   int N, K;
+  const void* packed;  /* optional unit-packed copy from sv_qmm_pack (device, 16-byte aligned), or NULL */
 } sv_qweight;
 typedef struct {
   sv_qweight qkv, o, gate_up, down;
@@ -263,6 +264,22 @@ typedef struct {
 } sv_model;
 
 size_t sv_round_workspace_bytes(const sv_model* model, int rows);
+
+/* Unit-packed weights (optional, for sv_verify_round).  The verify matmul
+ * streams a weight in units of 64 rows x 512 k; sv_qmm_pack writes a copy of
+ * one quantized weight [N, K] in which every unit is one contiguous block
+ * (the unit's codes in the shared-memory order the kernel reads, then its
+ * scales, then its biases; units tile-major, k-minor; rows beyond N padded
+ * with zeros), so the kernel fetches a unit with one bulk copy.  This is a
+ * relayout of the same bytes, done once outside the timed path; results are
+ * bitwise the same as from the canonical weight.  Set sv_qweight.packed to
+ * use it.  sv_qmm_pack_bytes returns ceil(N/64)*64 * K * (bits/8 + 4/64)
+ * bytes, or 0 for unsupported sizes (K a multiple of 512).  sv_qmm_pack
+ * validates like sv_qmm_verify, launches one kernel on `stream`, and writes
+ * only `packed` (caller-owned device memory, 16-byte aligned). */
+size_t sv_qmm_pack_bytes(int N, int K, int bits);
+int sv_qmm_pack(const uint32_t* wq, const uint16_t* scales, const uint16_t* biases, int N, int K, int bits, int group,
+                void* packed, size_t packed_bytes, void* stream);
 
 /* Round plan: the TMA descriptors of every projection of `model`, built once
  * per model in caller-owned device memory of sv_round_plan_bytes(model) bytes

@@ -29,7 +29,7 @@ _c_i32_p = ctypes.POINTER(ctypes.c_int32)
 
 class QWeight(ctypes.Structure):
     _fields_ = [("wq", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("biases", ctypes.c_void_p),
-                ("N", ctypes.c_int), ("K", ctypes.c_int)]
+                ("N", ctypes.c_int), ("K", ctypes.c_int), ("packed", ctypes.c_void_p)]
 
 
 class Layer(ctypes.Structure):
@@ -64,6 +64,9 @@ _SIGNATURES = {
                                 _c_void_p, _c_int, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_size_t,
                                 _c_void_p]),
     "sv_round_workspace_bytes": (_c_size_t, [_c_model_p, _c_int]),
+    "sv_qmm_pack_bytes": (_c_size_t, [_c_int, _c_int, _c_int]),
+    "sv_qmm_pack": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_int, _c_int, _c_int, _c_int, _c_void_p, _c_size_t,
+                             _c_void_p]),
     "sv_round_plan_bytes": (_c_size_t, [_c_model_p]),
     "sv_round_plan_init": (_c_int, [_c_model_p, _c_void_p, _c_size_t]),
     "sv_verify_round": (_c_int, [_c_model_p, _c_void_p, _c_int, _c_i32_p, _c_void_p, _c_int, _c_float, _c_void_p, _c_int,
@@ -237,8 +240,9 @@ class Library:
 
         ``layers``: list of dicts with keys qkv, o, gate_up, down."""
         def qw(w):
+            packed = w.get("packed")
             return QWeight(w["wq"].data_ptr(), w["scales"].data_ptr(), w["biases"].data_ptr(), w["wq"].shape[0],
-                           w["K"])
+                           w["K"], packed.data_ptr() if packed is not None else None)
         arr = (Layer * len(layers))(*[Layer(qw(l["qkv"]), qw(l["o"]), qw(l["gate_up"]), qw(l["down"]))
                                       for l in layers])
         m = Model(len(layers), hidden, q_dim, inter, vocab, bits, rms_eps, arr, qw(lm_head))
@@ -250,6 +254,18 @@ class Library:
         m.plan = self.workspace(nbytes, device=lm_head["wq"].device)
         self.check(self.lib.sv_round_plan_init(ctypes.byref(m), _ptr(m.plan), nbytes))
         return m
+
+    def pack(self, w, stream=None):
+        """Unit-packed copy of a device weight dict (sv_qmm_pack); returns a uint8 device tensor."""
+        import torch
+        N, K, bits = w["wq"].shape[0], w["K"], w["bits"]
+        nbytes = self.lib.sv_qmm_pack_bytes(N, K, bits)
+        if nbytes == 0:
+            raise SVError(SV_EUNSUPPORTED, "sv_qmm_pack_bytes: unsupported shape")
+        out = torch.empty(nbytes, dtype=torch.uint8, device=w["wq"].device)
+        self.check(self.lib.sv_qmm_pack(_ptr(w["wq"]), _ptr(w["scales"]), _ptr(w["biases"]), N, K, bits, 64, _ptr(out),
+                                        nbytes, _stream(stream)))
+        return out
 
     def round_workspace_bytes(self, model, rows):
         return self.lib.sv_round_workspace_bytes(ctypes.byref(model), rows)

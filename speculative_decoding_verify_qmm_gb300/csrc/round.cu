@@ -58,6 +58,7 @@ static int check_proj(const sv_qweight& w, int N, int K, int bits, int M, const 
   }
   if ((N >= 0 && w.N != N) || w.K != K)
     return fail(SV_EINVAL, "layer %d %s: shape %dx%d, expected %dx%d", layer, what, w.N, w.K, N, K);
+  if (w.packed && !aligned(w.packed, 16)) return fail(SV_EINVAL, "layer %d %s: packed weight not 16-byte aligned", layer, what);
   return SV_OK;
 }
 
@@ -85,6 +86,7 @@ static int check_model(const sv_model* md, int M) {
 static void set_phase(Phase& ph, const sv_qweight& w, int kind, int in_buf, int out_buf) {
   memset(&ph, 0, sizeof(ph));
   ph.wq = reinterpret_cast<const uint8_t*>(w.wq);
+  ph.packed = static_cast<const uint8_t*>(w.packed);
   ph.scales = w.scales;
   ph.biases = w.biases;
   ph.N = w.N;

@@ -64,11 +64,13 @@ struct StreamCfg {
   static constexpr int X_BYTES = MP * KC * 2;
   static constexpr int XS_BYTES = GPS * 2 * MP * 4;  // per group: scaled sums, then 2^-e
   static constexpr int SB_BYTES = BN * GPS * 2;
-  static constexpr int X_OFF = W_BYTES;
-  static constexpr int XS_OFF = X_OFF + X_BYTES;
-  static constexpr int S_OFF = (XS_OFF + XS_BYTES + 127) / 128 * 128;
+  // stage: [codes][scales][biases] (one packed unit, or three TMA boxes) then [activations][group sums]
+  static constexpr int S_OFF = W_BYTES;
   static constexpr int B_OFF = S_OFF + SB_BYTES;
-  static constexpr int STAGE_BYTES = (B_OFF + SB_BYTES + 1023) / 1024 * 1024;  // swizzle atoms 1024-aligned
+  static constexpr int UNIT_BYTES = B_OFF + SB_BYTES;  // one unit of a packed weight
+  static constexpr int X_OFF = UNIT_BYTES;
+  static constexpr int XS_OFF = X_OFF + X_BYTES;
+  static constexpr int STAGE_BYTES = (XS_OFF + XS_BYTES + 1023) / 1024 * 1024;  // swizzle atoms 1024-aligned
   static constexpr int RED_FLOATS = 16 * MP;        // one quarter's 16 rows
   static constexpr int RED_BYTES = 2 * 4 * RED_FLOATS * 4;  // result slot x quarter
   static constexpr int EPI_BYTES = 4 * 4 * MP * 4 + 256;    // cross-quarter scratch
@@ -707,10 +709,14 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
                 for (int k = 0; k < 3; ++k) prefetch_tensormap(maps_of(it.phase + 1) + k);
               mapped = it.phase;
             }
-            mbar_arrive_expect_tx(&full_bar[sg], C::W_BYTES + 2 * C::SB_BYTES);
-            tma_load_3d(st, tm, &full_bar[sg], 0, tile * BN, kc * C::ATOMS, pol_w);  // all pieces of the stage
-            tma_load_2d(st + C::S_OFF, tm + 1, &full_bar[sg], kc * GPS, tile * BN, pol_w);
-            tma_load_2d(st + C::B_OFF, tm + 2, &full_bar[sg], kc * GPS, tile * BN, pol_w);
+            mbar_arrive_expect_tx(&full_bar[sg], C::UNIT_BYTES);
+            if (ph.packed) {  // one contiguous unit: codes already swizzled, then scales, biases
+              bulk_load(st, ph.packed + (size_t)it.u * C::UNIT_BYTES, C::UNIT_BYTES, &full_bar[sg], pol_w);
+            } else {
+              tma_load_3d(st, tm, &full_bar[sg], 0, tile * BN, kc * C::ATOMS, pol_w);  // all pieces of the stage
+              tma_load_2d(st + C::S_OFF, tm + 1, &full_bar[sg], kc * GPS, tile * BN, pol_w);
+              tma_load_2d(st + C::B_OFF, tm + 2, &full_bar[sg], kc * GPS, tile * BN, pol_w);
+            }
           } else {
             const ActBuf& a = p.act[ph.in_buf];
             mbar_arrive_expect_tx(&full_bar[sg], C::X_BYTES + C::XS_BYTES);

@@ -44,6 +44,7 @@ enum PhaseKind : int {
 };
 
 struct Phase {
+  const uint8_t* packed;  // the weight in unit-packed form (sv_qmm_pack), or null: tensor maps
   const uint8_t* wq;
   const uint16_t* scales;
   const uint16_t* biases;
@@ -102,6 +103,7 @@ int prepare_into(const uint16_t* x, int ldx, int M, int K, int bits, int mode, c
                  const uint16_t* w, float eps, const ActBuf& out, cudaStream_t s);
 
 int device_sm_count();
+size_t packed_bytes(int N, int K, int bits);
 // Tensor maps of one quantized weight: codes in 128-byte swizzled boxes of
 // 64 rows, scales and biases in 8-group x 64-row boxes.
 int encode_weight_maps(CUtensorMap (&out)[3], const void* wq, const void* scales, const void* biases, int N, int K,

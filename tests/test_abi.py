@@ -110,3 +110,17 @@ def test_round_plan_argument_errors_on_host(raw):
     model.n_layers = 1
     assert raw.sv_round_plan_bytes(ctypes.byref(model)) == 5 * 3 * 128     # 5 projections x 3 descriptors
     assert raw.sv_round_plan_init(ctypes.byref(model), P(256), 1 << 20) == binding.SV_EINVAL  # null weights
+
+
+def test_pack_sizes_and_argument_errors_on_host(raw):
+    assert raw.sv_qmm_pack_bytes(1000, 1024, 8) == 16 * 2 * (64 * 512 + 2 * 64 * 8 * 2)
+    assert raw.sv_qmm_pack_bytes(1024, 1024, 4) == 16 * 2 * (64 * 256 + 2 * 64 * 8 * 2)
+    assert raw.sv_qmm_pack_bytes(1024, 576, 8) == 0      # K not a multiple of 512
+    assert raw.sv_qmm_pack_bytes(1024, 1024, 3) == 0
+    assert raw.sv_qmm_pack_bytes(0, 1024, 8) == 0
+    ok = dict(wq=P(256), s=P(256), b=P(256))
+    assert raw.sv_qmm_pack(None, ok["s"], ok["b"], 64, 512, 8, 64, P(256), 1 << 20, None) == binding.SV_EINVAL
+    assert raw.sv_qmm_pack(ok["wq"], ok["s"], ok["b"], 64, 512, 8, 64, None, 1 << 20, None) == binding.SV_EINVAL
+    assert raw.sv_qmm_pack(ok["wq"], ok["s"], ok["b"], 64, 512, 8, 64, P(264), 1 << 20, None) == binding.SV_EINVAL
+    assert raw.sv_qmm_pack(ok["wq"], ok["s"], ok["b"], 64, 512, 8, 64, P(256), 16, None) == binding.SV_EINVAL
+    assert raw.sv_qmm_pack(ok["wq"], ok["s"], ok["b"], 64, 512, 2, 64, P(256), 1 << 20, None) == binding.SV_EUNSUPPORTED

@@ -114,6 +114,71 @@ def test_batched_round_four_requests(lib):
         assert (int(n[b]), toks[offs[b]:offs[b] + n[b]].tolist()) == tuple(want[b])
 
 
+def _unpack_host(packed, N, K, bits):
+    """Canonical (codes bytes [N, K*bits/8], scales, biases) read back from a unit-packed buffer,
+    following the layout sv_qmm_pack documents: per (tile, chunk) unit, 128-byte pieces x 64 rows
+    with 16-byte chunk c of row r at c ^ (r & 7), then 64 x 8 scales, then 64 x 8 biases."""
+    rb = 512 * bits // 8
+    wbytes, sb = 64 * rb, 64 * 8 * 2
+    unit = wbytes + 2 * sb
+    tiles, upt = (N + 63) // 64, K // 512
+    buf = packed.cpu().numpy()
+    codes = np.zeros((tiles * 64, K * bits // 8), np.uint8)
+    sc = np.zeros((tiles * 64, K // 64), np.uint16)
+    bi = np.zeros((tiles * 64, K // 64), np.uint16)
+    for u in range(tiles * upt):
+        t, kc = divmod(u, upt)
+        blk = buf[u * unit:(u + 1) * unit]
+        for r in range(64):
+            for j in range(rb // 16):
+                piece, c = divmod(j, 8)
+                off = piece * 8192 + r * 128 + ((c ^ (r & 7)) << 4)
+                codes[t * 64 + r, kc * rb + 16 * j: kc * rb + 16 * j + 16] = blk[off:off + 16]
+        sc[t * 64:(t + 1) * 64, kc * 8:(kc + 1) * 8] = blk[wbytes:wbytes + sb].view(np.uint16).reshape(64, 8)
+        bi[t * 64:(t + 1) * 64, kc * 8:(kc + 1) * 8] = blk[wbytes + sb:].view(np.uint16).reshape(64, 8)
+    return codes, sc, bi
+
+
+@pytest.mark.parametrize("bits,N", [(8, 1000), (4, 1024)])
+def test_pack_layout_round_trips(lib, bits, N):
+    """The packed buffer holds exactly the canonical bytes in the documented order, zero rows past N."""
+    r = synthetic.rng(1480 + bits)
+    K = 1024
+    w = _model.to_device(synthetic.quant_weight(r, N, K, bits, synthetic.LARGE_8BIT))
+    packed = lib.pack(w)
+    torch.cuda.synchronize()
+    assert packed.numel() == lib.lib.sv_qmm_pack_bytes(N, K, bits) == ((N + 63) // 64) * 64 * K * (bits / 8 + 4 / 64)
+    codes, sc, bi = _unpack_host(packed, N, K, bits)
+    assert np.array_equal(codes[:N], w["wq"].cpu().numpy().view(np.uint8).reshape(N, -1))
+    assert np.array_equal(sc[:N], w["scales"].cpu().numpy().view(np.uint16))
+    assert np.array_equal(bi[:N], w["biases"].cpu().numpy().view(np.uint16))
+    assert not codes[N:].any() and not sc[N:].any() and not bi[N:].any()
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_packed_round_is_bitwise_the_canonical_round(lib, bits):
+    layers, head = _model.host_model(1490 + bits, 2, bits=bits,
+                                     stats=synthetic.TINY_4BIT if bits == 4 else synthetic.LARGE_8BIT, **TINY)
+    dl, dh = _model.device_layers(layers), _model.to_device(head)
+    canon = lib.make_model(dl, dh, TINY["hidden"], TINY["q_dim"], TINY["inter"], TINY["vocab"], bits)
+    pl = [{k: dict(v, packed=lib.pack(v)) for k, v in layer.items()} for layer in dl]
+    ph = dict(dh, packed=lib.pack(dh))
+    packed = lib.make_model(pl, ph, TINY["hidden"], TINY["q_dim"], TINY["inter"], TINY["vocab"], bits)
+    r = synthetic.rng(1495)
+    m = 7
+    h0 = dev_bf16(synthetic.activations(r, m + 1, TINY["hidden"]))
+    _, z_q = synthetic.logits_and_draft_probs(r, m, TINY["vocab"])
+    q = torch.from_numpy(z_q).cuda()
+    draft = torch.from_numpy(synthetic.sample_drafts(r, z_q)).cuda()
+    u = torch.from_numpy(synthetic.accept_uniforms(r, m + 1)).cuda()
+    for T in (0.0, 0.7):
+        a = _round(lib, canon, [0, m + 1], h0, T, q=q if T else None, draft=draft, u=u if T else None)
+        b = _round(lib, packed, [0, m + 1], h0, T, q=q if T else None, draft=draft, u=u if T else None)
+        assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+        assert np.array_equal(a[2], b[2]) and np.array_equal(a[3], b[3])
+    assert lib.device_error() == 0
+
+
 def test_round_refuses_a_plan_built_for_another_model(lib):
     layers, head = _model.host_model(1450, 1, bits=4, stats=synthetic.TINY_4BIT, **TINY)
     dl, dh = _model.device_layers(layers), _model.to_device(head)
