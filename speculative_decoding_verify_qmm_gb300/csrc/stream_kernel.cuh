@@ -421,7 +421,7 @@ __device__ __forceinline__ bool wait_counter(const int* ctr, int want, volatile 
 // both (`pair_here`); otherwise the up tile's finisher publishes its values and
 // the gate tile's finisher, which meets its tile later, combines the two.
 template <int BITS, int NT>
-__device__ void finish_tile(const StreamParams& p, const Phase& ph, int tile, int pair_here, int q, int lane,
+__device__ void finish_tile(const StreamParams& p, const Phase& ph, const ActBuf& out, int tile, int pair_here, int q, int lane,
                             float (&tot)[NT][4], const float (&rf)[NT][2], const float (&pre)[NT][4],
                             float (&g_keep)[NT][4], EpiScratch& es) {
   constexpr int MP = 8 * NT;
@@ -539,7 +539,7 @@ __device__ void finish_tile(const StreamParams& p, const Phase& ph, int tile, in
         const float u = is_up ? yv[j][e] : pre[j][e];
         yv[j][e] = m < p.M ? __bfloat162float(__float2bfloat16_rn(g / (1.f + expf(-g)) * u)) : 0.f;
       }
-    prepare_group<BITS, NT>(p, p.act[ph.out_buf], blk, ph.half, q, lane, yv, false, -1.f, es);
+    prepare_group<BITS, NT>(p, out, blk, ph.half, q, lane, yv, false, -1.f, es);
     return;
   }
 
@@ -559,7 +559,7 @@ __device__ void finish_tile(const StreamParams& p, const Phase& ph, int tile, in
         }
         yv[j][e] = v;
       }
-    if (ph.out_buf >= 0) prepare_group<BITS, NT>(p, p.act[ph.out_buf], tile, ph.N, q, lane, yv, true, p.rms_eps, es);
+    if (ph.out_buf >= 0) prepare_group<BITS, NT>(p, out, tile, ph.N, q, lane, yv, true, p.rms_eps, es);
     return;
   }
 
@@ -575,7 +575,7 @@ __device__ void finish_tile(const StreamParams& p, const Phase& ph, int tile, in
       yv[j][e] = m < p.M ? __bfloat162float(v) : 0.f;
     }
   if (tile < ph.prep_tiles)
-    prepare_group<BITS, NT>(p, p.act[ph.out_buf], tile, ph.prep_tiles * BN, q, lane, yv, false, -1.f, es);
+    prepare_group<BITS, NT>(p, out, tile, ph.prep_tiles * BN, q, lane, yv, false, -1.f, es);
 }
 
 // RMSNorm row factors 1/sqrt(mean(x^2) + eps) of the phase input for this
@@ -661,6 +661,14 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
     bool pdl_done = !is_x;     // the weight warp never reads what the previous kernel wrote
     unsigned long long t_wait = 0;
     bool bad = false;
+    // per-unit work reads only registers: the phase table lives in the
+    // kernel's parameter block, whose reads can miss the constant cache
+    struct {
+      int phase = -1, upt = 1;
+      const uint8_t* packed = nullptr;
+      const __half* xp = nullptr;
+      const float* xs = nullptr;
+    } cur;
     auto maps_of = [&](int phase) -> const CUtensorMap* { return p.maps ? p.maps + 3 * phase : p.tm; };
     while (!it.done(p)) {
       bool go = false;
@@ -697,9 +705,16 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
         }
       }
       if (go) {
-        if (lane == 0) {
+        if (it.phase != cur.phase) {  // the phase's fields, read from the parameter block once per phase
           const Phase& ph = p.ph[it.phase];
-          const int upt = ph.K / KC, kc = it.u % upt, sg = n % S;
+          cur.phase = it.phase;
+          cur.upt = ph.K / KC;
+          cur.packed = ph.packed;
+          cur.xp = p.act[ph.in_buf].xp;
+          cur.xs = p.act[ph.in_buf].xs;
+        }
+        if (lane == 0) {
+          const int upt = cur.upt, kc = it.u % upt, sg = n % S;
           uint8_t* st = smem + sg * C::STAGE_BYTES;
           if (!is_x) {
             const int tile = it.u / upt;
@@ -710,18 +725,17 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
               mapped = it.phase;
             }
             mbar_arrive_expect_tx(&full_bar[sg], C::UNIT_BYTES);
-            if (ph.packed) {  // one contiguous unit: codes already swizzled, then scales, biases
-              bulk_load(st, ph.packed + (size_t)it.u * C::UNIT_BYTES, C::UNIT_BYTES, &full_bar[sg], pol_w);
+            if (cur.packed) {  // one contiguous unit: codes already swizzled, then scales, biases
+              bulk_load(st, cur.packed + (size_t)it.u * C::UNIT_BYTES, C::UNIT_BYTES, &full_bar[sg], pol_w);
             } else {
               tma_load_3d(st, tm, &full_bar[sg], 0, tile * BN, kc * C::ATOMS, pol_w);  // all pieces of the stage
               tma_load_2d(st + C::S_OFF, tm + 1, &full_bar[sg], kc * GPS, tile * BN, pol_w);
               tma_load_2d(st + C::B_OFF, tm + 2, &full_bar[sg], kc * GPS, tile * BN, pol_w);
             }
           } else {
-            const ActBuf& a = p.act[ph.in_buf];
             mbar_arrive_expect_tx(&full_bar[sg], C::X_BYTES + C::XS_BYTES);
-            bulk_load(st + C::X_OFF, a.xp + (size_t)kc * (KC / 32) * MP * 32, C::X_BYTES, &full_bar[sg], pol_x);
-            bulk_load(st + C::XS_OFF, a.xs + (size_t)kc * GPS * 2 * MP, C::XS_BYTES, &full_bar[sg], pol_x);
+            bulk_load(st + C::X_OFF, cur.xp + (size_t)kc * (KC / 32) * MP * 32, C::X_BYTES, &full_bar[sg], pol_x);
+            bulk_load(st + C::XS_OFF, cur.xs + (size_t)kc * GPS * 2 * MP, C::XS_BYTES, &full_bar[sg], pol_x);
           }
         }
         __syncwarp();
@@ -771,7 +785,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
     zero4<NT>(tot);
     int i = 0, n_te = 0;  // units consumed, tile ends handed over
     for (int ph_i = 0; ph_i < p.n_phases; ++ph_i) {
-      const Phase& ph = p.ph[ph_i];
+      const Phase ph = p.ph[ph_i];
       const int upt = ph.K / KC, total = ph_units(ph);
       const int pg = phase_grid(ph, p.grid);
       const int u0 = unit_start(blockIdx.x, total, pg), u1 = unit_start(blockIdx.x + 1, total, pg);
@@ -825,7 +839,12 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
   zero4<NT>(g_keep);
   int n_te = 0;
   for (int ph_i = 0; ph_i < p.n_phases; ++ph_i) {
-    const Phase& ph = p.ph[ph_i];
+    // the phase's fields and buffers, read from the parameter block once per
+    // phase (before its barrier opens) instead of at every use in the tail
+    const Phase ph = p.ph[ph_i];
+    const ActBuf in_a = p.act[ph.in_buf];
+    ActBuf out_a = {};
+    if (ph.out_buf >= 0) out_a = p.act[ph.out_buf];
     const int upt = ph.K / KC, total = ph_units(ph);
     const int pg = phase_grid(ph, p.grid);
     const int u0 = unit_start(blockIdx.x, total, pg), u1 = unit_start(blockIdx.x + 1, total, pg);
@@ -838,7 +857,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
           __nanosleep(32);
         }
       }
-      rms_factors<NT>(p.act[ph.in_buf], ph.K, lane, rf);
+      rms_factors<NT>(in_a, ph.K, lane, rf);
       const int first_tile = u0 / upt, last_tile = (u1 - 1) / upt;
       for (int tile = first_tile; tile <= last_tile; ++tile) {
         const int fin = tile_finisher(tile, upt, total, pg);
@@ -903,7 +922,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
             for (int e = 0; e < 4; ++e) tot[j][e] += part[j][e];
           if (q == 0 && lane == 0) p.tile_counters[tile] = 0;
         }
-        finish_tile<BITS, NT>(p, ph, tile, pair_here, q, lane, tot, rf, pre, g_keep, es);
+        finish_tile<BITS, NT>(p, ph, out_a, tile, pair_here, q, lane, tot, rf, pre, g_keep, es);
       }
     }
     // phase done: the epilogue warps' writes (which other CTAs read through
