@@ -651,6 +651,10 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
     // warps: one lane completes only a few copy instructions per
     // microsecond.  Each arrives once per stage use on the stage's full
     // barrier (count 2) with its own byte count.
+    // one lane issues: the others leave at once, so no per-unit step of the
+    // loop needs a shuffle or a warp barrier (each of those queues behind the
+    // consumers' shared-memory traffic)
+    if (lane != 0) return;
     const bool is_x = warp == XPW;
     const uint64_t pol_w = l2_evict_first(), pol_x = l2_evict_last();
     UnitIter it;
@@ -673,12 +677,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
     while (!it.done(p)) {
       bool go = false;
       // the stage must be free: its previous unit consumed
-      bool free_slot = n < S;
-      if (!free_slot) {
-        int ok = 0;
-        if (lane == 0) ok = mbar_test_wait(&empty_bar[n % S], ((n / S) - 1) & 1);
-        free_slot = __shfl_sync(0xffffffffu, ok, 0);
-      }
+      bool free_slot = n < S || mbar_test_wait(&empty_bar[n % S], ((n / S) - 1) & 1);
       if (free_slot) {
         if (!is_x) {
           go = true;
@@ -688,20 +687,14 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
           continue;
         } else if (it.phase <= ready) {
           go = true;
-        } else {
+        } else if (ld_acquire(p.grid_bar + it.phase) >= (unsigned)p.grid) {
           // grid barrier of this unit's phase: one counter per transition, so
           // CTAs that skip ahead through phases in which they have no units
           // cannot stand in for CTAs still working
-          int pass = 0;
-          if (lane == 0 && ld_acquire(p.grid_bar + it.phase) >= (unsigned)p.grid) {
-            fence_proxy_async();
-            pass = 1;
-          }
-          if (__shfl_sync(0xffffffffu, pass, 0)) {
-            ready = it.phase;
-            if (lane == 0) st_release_cta(&ready_ph, ready);
-            go = true;
-          }
+          fence_proxy_async();
+          ready = it.phase;
+          st_release_cta(&ready_ph, ready);
+          go = true;
         }
       }
       if (go) {
@@ -713,32 +706,29 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
           cur.xp = p.act[ph.in_buf].xp;
           cur.xs = p.act[ph.in_buf].xs;
         }
-        if (lane == 0) {
-          const int upt = cur.upt, kc = it.u % upt, sg = n % S;
-          uint8_t* st = smem + sg * C::STAGE_BYTES;
-          if (!is_x) {
-            const int tile = it.u / upt;
-            const CUtensorMap* tm = maps_of(it.phase);
-            if (it.phase != mapped) {  // warm the descriptor cache for this phase and the next
-              if (it.phase + 1 < p.n_phases && p.maps)
-                for (int k = 0; k < 3; ++k) prefetch_tensormap(maps_of(it.phase + 1) + k);
-              mapped = it.phase;
-            }
-            mbar_arrive_expect_tx(&full_bar[sg], C::UNIT_BYTES);
-            if (cur.packed) {  // one contiguous unit: codes already swizzled, then scales, biases
-              bulk_load(st, cur.packed + (size_t)it.u * C::UNIT_BYTES, C::UNIT_BYTES, &full_bar[sg], pol_w);
-            } else {
-              tma_load_3d(st, tm, &full_bar[sg], 0, tile * BN, kc * C::ATOMS, pol_w);  // all pieces of the stage
-              tma_load_2d(st + C::S_OFF, tm + 1, &full_bar[sg], kc * GPS, tile * BN, pol_w);
-              tma_load_2d(st + C::B_OFF, tm + 2, &full_bar[sg], kc * GPS, tile * BN, pol_w);
-            }
-          } else {
-            mbar_arrive_expect_tx(&full_bar[sg], C::X_BYTES + C::XS_BYTES);
-            bulk_load(st + C::X_OFF, cur.xp + (size_t)kc * (KC / 32) * MP * 32, C::X_BYTES, &full_bar[sg], pol_x);
-            bulk_load(st + C::XS_OFF, cur.xs + (size_t)kc * GPS * 2 * MP, C::XS_BYTES, &full_bar[sg], pol_x);
+        const int upt = cur.upt, kc = it.u % upt, sg = n % S;
+        uint8_t* st = smem + sg * C::STAGE_BYTES;
+        if (!is_x) {
+          const int tile = it.u / upt;
+          const CUtensorMap* tm = maps_of(it.phase);
+          if (it.phase != mapped) {  // warm the descriptor cache for this phase and the next
+            if (it.phase + 1 < p.n_phases && p.maps)
+              for (int k = 0; k < 3; ++k) prefetch_tensormap(maps_of(it.phase + 1) + k);
+            mapped = it.phase;
           }
+          mbar_arrive_expect_tx(&full_bar[sg], C::UNIT_BYTES);
+          if (cur.packed) {  // one contiguous unit: codes already swizzled, then scales, biases
+            bulk_load(st, cur.packed + (size_t)it.u * C::UNIT_BYTES, C::UNIT_BYTES, &full_bar[sg], pol_w);
+          } else {
+            tma_load_3d(st, tm, &full_bar[sg], 0, tile * BN, kc * C::ATOMS, pol_w);  // all pieces of the stage
+            tma_load_2d(st + C::S_OFF, tm + 1, &full_bar[sg], kc * GPS, tile * BN, pol_w);
+            tma_load_2d(st + C::B_OFF, tm + 2, &full_bar[sg], kc * GPS, tile * BN, pol_w);
+          }
+        } else {
+          mbar_arrive_expect_tx(&full_bar[sg], C::X_BYTES + C::XS_BYTES);
+          bulk_load(st + C::X_OFF, cur.xp + (size_t)kc * (KC / 32) * MP * 32, C::X_BYTES, &full_bar[sg], pol_x);
+          bulk_load(st + C::XS_OFF, cur.xs + (size_t)kc * GPS * 2 * MP, C::XS_BYTES, &full_bar[sg], pol_x);
         }
-        __syncwarp();
         it.next(p);
         ++n;
         t_wait = 0;
@@ -750,15 +740,10 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
       __nanosleep(32);
       const unsigned long long now = global_ns();
       if (!t_wait) t_wait = now;
-      int stop = 0;
-      if (now - t_wait > 20000ull && lane == 0) stop = (*abort_v | *abort_g) || (now - t_wait > WAIT_LIMIT_NS);
-      stop = __shfl_sync(0xffffffffu, stop, 0);
-      if (stop) {
-        if (lane == 0) {
-          if (!(*abort_v | *abort_g)) raise_error(ERR_TIMEOUT_EMPTY);
-          *abort_v = 1;
-          *abort_g = 1;
-        }
+      if (now - t_wait > 20000ull && ((*abort_v | *abort_g) || now - t_wait > WAIT_LIMIT_NS)) {
+        if (!(*abort_v | *abort_g)) raise_error(ERR_TIMEOUT_EMPTY);
+        *abort_v = 1;
+        *abort_g = 1;
         bad = true;
         break;
       }
@@ -766,14 +751,12 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
     // drain copies already issued into the ring before the CTA may exit; after
     // an abort a stage may never complete, so give its copies a fixed 50 us
     // to land instead
-    if (lane == 0) {
-      if (!bad && !*abort_v) {
-        for (int k = (n - S > 0 ? n - S : 0); k < n; ++k)
-          mbar_wait_bounded(&full_bar[k % S], (k / S) & 1, abort_v);
-      } else {
-        const unsigned long long t0 = global_ns();
-        while (global_ns() - t0 < 50000ull) __nanosleep(1000);
-      }
+    if (!bad && !*abort_v) {
+      for (int k = (n - S > 0 ? n - S : 0); k < n; ++k)
+        mbar_wait_bounded(&full_bar[k % S], (k / S) & 1, abort_v);
+    } else {
+      const unsigned long long t0 = global_ns();
+      while (global_ns() - t0 < 50000ull) __nanosleep(1000);
     }
     return;
   }
