@@ -55,6 +55,10 @@
 
 namespace sv {
 
+#ifndef RUN_AHEAD_M8
+#define RUN_AHEAD_M8 2
+#endif
+
 template <int BITS, int NT>
 struct StreamCfg {
   static constexpr int MP = 8 * NT;
@@ -78,6 +82,11 @@ struct StreamCfg {
   static constexpr int STAGES_FIT = BUDGET / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + RED_BYTES + EPI_BYTES;
+  // units of a phase whose grid barrier has not opened that the weight warp
+  // may copy ahead: more copies in flight while a transition's chain of L2
+  // round trips (split-tile fixup, barrier, first activation copy) runs slow
+  // that chain down by more than they save (measured at M <= 8)
+  static constexpr int RUN_AHEAD = NT == 1 ? RUN_AHEAD_M8 : STAGES;
   static_assert(STAGES >= 2, "stage ring too small");
   static_assert(SMEM + 2048 <= 227 * 1024, "shared memory budget");
   static_assert(W_BYTES % 1024 == 0 && X_OFF % 16 == 0 && XS_OFF % 16 == 0 && S_OFF % 128 == 0 &&
@@ -660,6 +669,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
     UnitIter it;
     it.start(p, 0);
     int n = 0;                 // units issued so far by this warp
+    int ahead_ph = -1, ahead_n = 0;  // (weight warp) units issued of the newest phase not yet open
     int ready = 0;             // (activation warp) highest phase whose activations may be loaded
     int mapped = -1;           // (weight warp) last phase whose tensor maps were prefetched
     bool pdl_done = !is_x;     // the weight warp never reads what the previous kernel wrote
@@ -678,6 +688,14 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
       bool go = false;
       // the stage must be free: its previous unit consumed
       bool free_slot = n < S || mbar_test_wait(&empty_bar[n % S], ((n / S) - 1) & 1);
+      if (free_slot && !is_x && it.phase > ld_acquire_cta(&ready_ph)) {
+        if (ahead_ph != it.phase) {
+          ahead_ph = it.phase;
+          ahead_n = 0;
+        }
+        free_slot = ahead_n < C::RUN_AHEAD;
+        ahead_n += free_slot;
+      }
       if (free_slot) {
         if (!is_x) {
           go = true;
