@@ -11,11 +11,13 @@
  *   - All array pointers are DEVICE pointers owned by the caller unless the
  *     parameter says "host".  The library allocates no device memory; calls
  *     that need scratch space take a caller-provided workspace whose size comes
- *     from the matching *_workspace_bytes() query, 256-byte aligned.  Every
- *     workspace starts with a 256 KiB block of counters that must be zero
- *     filled once after allocation (e.g. cudaMemsetAsync) and that every
- *     successful call leaves at zero again, so one workspace (sized for the
- *     largest call) can serve any sequence of calls ordered on one stream.
+ *     from the matching *_workspace_bytes() query, 256-byte aligned.  A
+ *     workspace must be zero filled once after allocation (e.g.
+ *     cudaMemsetAsync over all of it): it holds a 256 KiB block of counters
+ *     and the split-tile partial sums, which every successful call leaves at
+ *     zero again, so one workspace (sized for the largest call) can serve any
+ *     sequence of calls ordered on one stream.  After a call that reported a
+ *     device error, zero it again before reuse.
  *   - bf16 and fp16 values are passed as uint16_t bit patterns.
  *   - Matrices are row-major; ld* is the row stride in elements.
  *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the
@@ -245,7 +247,7 @@ int sv_swiglu(const uint16_t* g, int ldg, const uint16_t* u, int ldu, int M, int
  *     `stream` just before and after the launch that runs all the projections,
  *     for timing it (recording them adds a dependency that delays that launch
  *     by the previous launch's drain).
- * Workspace: sv_round_workspace_bytes(model, M) bytes (zero prefix rule above). */
+ * Workspace: sv_round_workspace_bytes(model, M) bytes (zero-fill rule above). */
 typedef struct {
   const uint32_t* wq;
   const uint16_t* scales;

@@ -240,6 +240,14 @@ size_t qmm_bytes(int M, int N, int K, int bits, bool stats) {
   return workspace_layout(M, K, grid, stats ? tiles : 0, 1).total;
 }
 
+void qmm_partials_region(int M, int N, int K, int bits, size_t* off, size_t* bytes) {
+  const int tiles = (N + BN - 1) / BN;
+  const int grid = grid_for(bits, M, tiles * (K / KC));
+  const Layout L = workspace_layout(M, K, grid > 0 ? grid : 0, 0, 1);
+  *off = L.partials;
+  *bytes = L.tile_stats - L.partials;
+}
+
 int qmm_run_internal(const uint32_t* wq, const uint16_t* scales, const uint16_t* biases, int N, int K, int bits,
                      int M, int mode, uint16_t* y, int ldy, const uint16_t* residual, int ldr, float* logits,
                      int ldl, float temperature, float* row_max, float* row_sumexp, int32_t* row_argmax, void* ws,

@@ -284,6 +284,60 @@ __device__ __forceinline__ void red_add(const float* buf, float (&v)[NT][4], int
     }
 }
 
+// Split-tile partial sums travel through global memory as self-announcing
+// words: a contributor stores each fp32 partial with all bits inverted, and
+// the finisher polls the words themselves (zero = not yet written), adds them
+// and zeroes them again for the next use.  No partial is ever the all-ones
+// pattern (arithmetic yields only the canonical NaN), so no written word
+// reads as zero; each 32-bit word is written and read whole, and the slot is
+// next written only after a grid barrier that follows the zeroing.
+template <int NT>
+__device__ __forceinline__ void partial_store(float* buf, const float (&v)[NT][4], int lane) {
+#pragma unroll
+  for (int j = 0; j < NT; ++j)
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      __stcg(reinterpret_cast<unsigned*>(buf) + (j * 4 + e) * 32 + lane, ~__float_as_uint(v[j][e]));
+}
+// Adds one contributor's partials (bounded wait; false on abort or timeout).
+template <int NT>
+__device__ __forceinline__ bool partial_take(float* buf, float (&v)[NT][4], int lane, volatile int* abort_v,
+                                             volatile int* abort_g) {
+  unsigned* w = reinterpret_cast<unsigned*>(buf);
+  unsigned got[NT][4];
+  const unsigned long long t0 = global_ns();
+  for (unsigned it = 0;; ++it) {
+    bool all = true;
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        got[j][e] = __ldcv(w + (j * 4 + e) * 32 + lane);
+        all &= got[j][e] != 0u;
+      }
+    if (all) break;
+    if ((it & 15u) == 15u) {
+      if (*abort_v) return false;
+      const unsigned long long dt = global_ns() - t0;
+      if (dt > 20000ull && *abort_g) return false;
+      if (dt > WAIT_LIMIT_NS) {
+        raise_error(ERR_TIMEOUT_FULL);
+        *abort_v = 1;
+        *abort_g = 1;
+        return false;
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < NT; ++j)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      v[j][e] += __uint_as_float(~got[j][e]);
+      __stcg(w + (j * 4 + e) * 32 + lane, 0u);
+    }
+  return true;
+}
+
 constexpr int EPI_BAR = 5;       // the four epilogue warps
 constexpr int EPI_THREADS = 128;
 
@@ -871,15 +925,11 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
         if (finisher) {
           // ---- fetch ahead: contributors' partials (they met this tile first)
           if (c_last != fin) {
-            int others = 0;
-            for (int c = fin + 1; c <= c_last; ++c) others += unit_start(c + 1, total, pg) > unit_start(c, total, pg);
-            int ok = 1;
-            if (q == 0 && lane == 0) ok = wait_counter(p.tile_counters + tile, others, abort_v, abort_g);
-            named_bar_sync(EPI_BAR, EPI_THREADS);
             for (int c = fin + 1; c <= c_last; ++c)
-              if (unit_start(c + 1, total, pg) > unit_start(c, total, pg))
-                red_add<NT, true>(p.partials + (((size_t)c * 2) * 4 + q) * C::RED_FLOATS, part, lane);
-            (void)ok;
+              if (unit_start(c + 1, total, pg) > unit_start(c, total, pg) &&
+                  !partial_take<NT>(p.partials + (((size_t)c * 2) * 4 + q) * C::RED_FLOATS, part, lane, abort_v,
+                                    abort_g))
+                break;
           }
           // ... the hidden-state rows of a residual tile, the partner of a gate tile
           if (ph.kind == PH_RESID) {
@@ -910,10 +960,8 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
         mbar_arrive(&res_empty[slot]);
         ++n_te;
         if (!finisher) {
-          // contributor: publish the partial sums, then count them
-          red_store<NT>(p.partials + (((size_t)blockIdx.x * 2) * 4 + q) * C::RED_FLOATS, tot, lane);
-          named_bar_sync(EPI_BAR, EPI_THREADS);
-          if (q == 0 && lane == 0) red_release_add(reinterpret_cast<unsigned*>(p.tile_counters + tile), 1u);
+          // contributor: publish the partial sums (the finisher polls them)
+          partial_store<NT>(p.partials + (((size_t)blockIdx.x * 2) * 4 + q) * C::RED_FLOATS, tot, lane);
           continue;
         }
         if (c_last != fin) {  // own sums first, then the contributors' in CTA order
@@ -921,7 +969,6 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
           for (int j = 0; j < NT; ++j)
 #pragma unroll
             for (int e = 0; e < 4; ++e) tot[j][e] += part[j][e];
-          if (q == 0 && lane == 0) p.tile_counters[tile] = 0;
         }
         finish_tile<BITS, NT>(p, ph, out_a, tile, pair_here, q, lane, tot, rf, pre, g_keep, es);
       }

@@ -116,6 +116,9 @@ size_t align256(size_t v);
 bool aligned(const void* p, size_t a);
 size_t prepare_bytes(int M, int K);
 size_t qmm_bytes(int M, int N, int K, int bits, bool stats);
+// Offset and size of the split-tile partials in a one-projection workspace
+// (zero between calls, like the counter block).
+void qmm_partials_region(int M, int N, int K, int bits, size_t* off, size_t* bytes);
 size_t accept_bytes(int B, int rows);
 int qmm_prepare_internal(const uint16_t* x, int ldx, int M, int K, int bits, int mode, const uint16_t* x2, int ldx2,
                          const uint16_t* w, float eps, void* ws, cudaStream_t s);
