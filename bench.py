@@ -291,8 +291,8 @@ def cpu_cores():
 # capture of a smaller round (profiles/stream_kernel_m8_4layers.md), scaled to
 # a full launch by weight bytes; valid only for the kernel source it was taken
 # on, so the source's hash is checked and the figure dropped when it differs.
-TRAFFIC_CAPTURE = {"sha256": "617c1c40a3b672269034baa9bc6981e246fb9835ac284f9fd401ecf619534967", "M": 8,
-                   "bytes": 1481500928 + 6686976, "weight_bytes": 1481211904}
+TRAFFIC_CAPTURE = {"sha256": "452bbfb45b4d729d6f33d394d345fcad075fc1266dc1c132967a66d1be7b9f3d", "M": 8,
+                   "bytes": 1481508352 + 6188544, "weight_bytes": 1481211904}
 
 
 def measured_traffic(M, wbytes):

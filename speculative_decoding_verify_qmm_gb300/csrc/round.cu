@@ -228,13 +228,6 @@ int sv_verify_round(const sv_model* model, const void* plan, int B, const int32_
   }
   set_phase(p.ph[n++], model->lm_head, PH_LOGITS, 0, -1);
   p.n_phases = n;
-  // Short projections (at most one tile per CTA, 8 k-chunks per tile) run
-  // whole tiles: most of a tile's weights are already in the CTA's ring when
-  // the phase opens, and an unsplit tile needs no cross-CTA reduction.
-  for (int i = 0; i < n; ++i) {
-    Phase& ph = p.ph[i];
-    ph.whole = (ph.N + BN - 1) / BN <= R.grid && ph.K / KC <= 8;
-  }
   p.logits = logits;
   p.ldl = ldl;
   p.inv_temp = temperature > 0.f ? 1.f / temperature : 0.f;

@@ -19,12 +19,12 @@
 // by 2^e per (row, group) so that every bf16 value keeps all its bits.
 //
 // Work and data flow (one CTA per SM; stream-K over (64-row tile, 512-k chunk)
-// units, so every SM streams the same number of weight bytes, except that
-// short phases of at most one tile per CTA give each CTA one whole tile):
+// units, so every SM streams the same number of weight bytes):
 //   * warps 8 and 13 (producers) fill a ring of shared-memory stages with TMA
-//     copies, warp 8 the weights and warp 13 the activations (a lane
-//     completes only a few copy instructions per microsecond, so the copies
-//     are few, large, and split over two warps): the tile's codes as one 3D
+//     copies, warp 8 the weights and warp 13 the activations (each step of a
+//     producer's loop waits behind the consumers' shared-memory traffic, so
+//     the copies are few, large, and split over two warps): from unit-packed
+//     weights one bulk copy per stage, otherwise the tile's codes as one 3D
 //     box of 128-byte pieces x 64 rows with the 128-byte swizzle (ldmatrix
 //     then reads them without bank conflicts), one 64 x 8 box each of scales
 //     and biases, and the matching slice of the prepared activations as plain
@@ -95,13 +95,10 @@ struct StreamCfg {
 
 // ------------------------------------------------------------ schedule math
 __device__ __forceinline__ int ph_units(const Phase& ph) { return ((ph.N + BN - 1) / BN) * (ph.K / KC); }
-// Units of a phase are split over `grid` CTAs in contiguous ranges (stream-K),
-// or, for a phase flagged whole-tile, one tile per CTA (grid = tiles; CTAs
-// beyond it get nothing), so that no tile is split.
+// Units of a phase are split over `grid` CTAs in contiguous ranges (stream-K).
 __device__ __forceinline__ int unit_start(int c, int total, int grid) {
-  return c >= grid ? total : static_cast<int>(static_cast<long long>(c) * total / grid);
+  return static_cast<int>(static_cast<long long>(c) * total / grid);
 }
-__device__ __forceinline__ int phase_grid(const Phase& ph, int grid) { return ph.whole ? (ph.N + BN - 1) / BN : grid; }
 __device__ __forceinline__ int unit_owner(long long u, int total, int grid) {
   return static_cast<int>(((u + 1) * grid - 1) / total);
 }
@@ -120,7 +117,7 @@ struct UnitIter {
       ++phase;
       if (phase >= p.n_phases) return;
       total = ph_units(p.ph[phase]);
-      const int g = phase_grid(p.ph[phase], p.grid);
+      const int g = p.grid;
       u = unit_start(blockIdx.x, total, g);
       u_end = unit_start(blockIdx.x + 1, total, g);
     } while (u >= u_end);
@@ -842,7 +839,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
     for (int ph_i = 0; ph_i < p.n_phases; ++ph_i) {
       const Phase ph = p.ph[ph_i];
       const int upt = ph.K / KC, total = ph_units(ph);
-      const int pg = phase_grid(ph, p.grid);
+      const int pg = p.grid;
       const int u0 = unit_start(blockIdx.x, total, pg), u1 = unit_start(blockIdx.x + 1, total, pg);
       for (int u = u0; u < u1; ++u, ++i) {
         const int kc = u % upt, s = i % S;
@@ -901,7 +898,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
     ActBuf out_a = {};
     if (ph.out_buf >= 0) out_a = p.act[ph.out_buf];
     const int upt = ph.K / KC, total = ph_units(ph);
-    const int pg = phase_grid(ph, p.grid);
+    const int pg = p.grid;
     const int u0 = unit_start(blockIdx.x, total, pg), u1 = unit_start(blockIdx.x + 1, total, pg);
     if (u0 < u1) {
       // this phase's inputs are complete once the producer passed its grid barrier

@@ -55,7 +55,6 @@ struct Phase {
   int prep_tiles;     // PH_STORE: output tiles that feed the next phase
   int in_buf, out_buf;
   int half;           // PH_GATEUP: columns per half (gate, then up) of y
-  int whole;          // one whole tile per CTA instead of stream-K (tiles <= grid)
 };
 
 // Prepared activations of one phase input (K <= the buffer's capacity).
