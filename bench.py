@@ -291,7 +291,7 @@ def cpu_cores():
 # capture of a smaller round (profiles/stream_kernel_m8_4layers.md), scaled to
 # a full launch by weight bytes; valid only for the kernel source it was taken
 # on, so the source's hash is checked and the figure dropped when it differs.
-TRAFFIC_CAPTURE = {"sha256": "452bbfb45b4d729d6f33d394d345fcad075fc1266dc1c132967a66d1be7b9f3d", "M": 8,
+TRAFFIC_CAPTURE = {"sha256": "0f292be305e8bd4d84ab514826071a6eedc221f1a39c5abd086ee7d7e9034684", "M": 8,
                    "bytes": 1481508352 + 6188544, "weight_bytes": 1481211904}
 
 

@@ -98,7 +98,6 @@ void stream_params_init(StreamParams& p, void* ws, const Layout& L, int M, int g
   p.act[0] = act_buf(ws, L, 0);
   p.act[1] = L.act[1][0] ? act_buf(ws, L, 1) : p.act[0];
   p.partials = reinterpret_cast<float*>(base + L.partials);
-  p.tile_counters = reinterpret_cast<int*>(base + TILE_CTR_OFF);
   p.pair_counters = reinterpret_cast<int*>(base + PAIR_CTR_OFF);
   p.grid_bar = reinterpret_cast<unsigned*>(base + GRID_BAR_OFF);
   p.exit_counter = reinterpret_cast<int*>(base + EXIT_CTR_OFF);
@@ -483,7 +482,7 @@ int accept_internal(int B, const int32_t* offs, const float* logits, int ldl, co
   p.out_len = out_len;
   p.out_tokens = out_tokens;
   p.chunk_sums = reinterpret_cast<double*>(base + accept_sums_offset());
-  p.counters = reinterpret_cast<int*>(base);
+  p.counters = reinterpret_cast<int*>(base + ACC_CTR_OFF);
   p.nb = accept_chunks(V);
   cudaError_t e = launch_accept(p, B, s);
   if (e != cudaSuccess) return cuda_fail(e, "accept launch");

@@ -68,15 +68,13 @@ int sv_qmm_verify_noalloc(const uint32_t* wq, const uint16_t* scales, const uint
   st = noalloc_scratch(&ws);
   if (st) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // The array keeps whatever the last call left; the tile counters and the
-  // split-tile partials must start at zero, so clear this call's (a failed
+  // The array keeps whatever the last call left; the exit and abort words and
+  // the split-tile partials must start at zero, so clear them (a failed
   // earlier call may have left them set).  No allocation: memsets of the
   // array itself.
-  const size_t counter_bytes = (size_t)((N + BN - 1) / BN) * 4;
   size_t part_off = 0, part_bytes = 0;
   qmm_partials_region(M, N, K, bits, &part_off, &part_bytes);
-  cudaError_t e = cudaMemsetAsync(ws, 0, counter_bytes, s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(static_cast<uint8_t*>(ws) + EXIT_CTR_OFF, 0, 8, s);  // exit, abort
+  cudaError_t e = cudaMemsetAsync(static_cast<uint8_t*>(ws) + EXIT_CTR_OFF, 0, 8, s);  // exit, abort
   if (e == cudaSuccess) e = cudaMemsetAsync(static_cast<uint8_t*>(ws) + part_off, 0, part_bytes, s);
   if (e != cudaSuccess) return cuda_fail(e, "clear scratch counters");
   st = qmm_prepare_internal(x, ldx, M, K, bits, PREP_PLAIN, nullptr, 0, nullptr, 0.f, ws, s);

@@ -29,8 +29,9 @@
 //     then reads them without bank conflicts), one 64 x 8 box each of scales
 //     and biases, and the matching slice of the prepared activations as plain
 //     bulk copies.  The weights run ahead into the next phase while the
-//     current phase drains; only the activation copies wait for the
-//     grid-wide phase barrier.
+//     current phase drains (at M <= 8 by at most two units: more copies in
+//     flight slow the transition itself); only the activation copies wait
+//     for the grid-wide phase barrier.
 //   * warps 0-7 (consumers) are 4 row quarters x 2 k halves: ldmatrix the codes,
 //     turn them into fp16 with byte-permute / LOP3, mma.sync m16n8k16 against
 //     the activation fragments, fold each group into fp32 sums.  At a tile's
@@ -38,9 +39,10 @@
 //     slots in shared memory, and the consumers go straight on to the next
 //     unit: nothing that waits on global memory runs on them.
 //   * warps 9-12 (epilogue, one per row quarter) finish each tile from its
-//     result slot.  A tile split across CTAs is finished by whichever
-//     contributor arrives last (atomic counter, no spinning), adding the
-//     partials in CTA order, so results are bitwise reproducible.  The
+//     result slot.  A tile split across CTAs is finished by the CTA whose
+//     range holds its first unit; the others reach the tile first and publish
+//     their partial sums as self-announcing words, which the finisher polls
+//     and adds in CTA order, so results are bitwise reproducible.  The
 //     finishing epilogue writes the phase output and prepares it as the next
 //     phase's input (fp16 scaling, group sums, RMSNorm statistics, SwiGLU of
 //     gate/up block pairs).

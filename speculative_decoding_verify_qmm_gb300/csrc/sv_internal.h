@@ -28,7 +28,7 @@ enum PrepMode : int { PREP_PLAIN = 0, PREP_RMSNORM = 1, PREP_SWIGLU = 2 };
 
 // Workspace prefix of counters that are zero between calls.
 constexpr size_t COUNTER_BYTES = 262144;
-constexpr size_t TILE_CTR_OFF = 0;            // per tile of the running phase
+constexpr size_t ACC_CTR_OFF = 0;             // the accept step's per-request counters
 constexpr int MAX_TILES = 32768;
 constexpr size_t PAIR_CTR_OFF = 131072;       // per gate/up block pair
 constexpr size_t GRID_BAR_OFF = 196608;       // grid barrier arrivals, one counter per phase transition
@@ -71,7 +71,6 @@ struct StreamParams {
   float rms_eps;
   ActBuf act[2];
   float* partials;        // [grid][2 slots][4 quarters][16*MP]
-  int* tile_counters;
   int* pair_counters;
   unsigned* grid_bar;     // [MAX_PHASES]: arrivals for the transition into phase t
   int* exit_counter;
