@@ -330,7 +330,7 @@ def main():
                           "lm_head 4096->151936 + spec_accept" % shape["n_layers"],
               "M": M, "m": M - 1, "temperature": TEMPERATURE, "draft_agreement": 0.7,
               "weight_bytes_per_round": wbytes, "l2": "no flush: %.2f GB of weights per round >> 129 MB L2" % (wbytes / 1e9),
-              "weight_layout": args.layout, "parallelism": "replicas" if args.gpus > 1 else "single GPU"}
+              "parallelism": "replicas" if args.gpus > 1 else "single GPU"}
 
     if args.impl == "reference":
         if rank != 0:
@@ -420,6 +420,7 @@ def main():
         "warmup": args.warmup, "ms_per_step": us[M] / 1e3, "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "q8 codes x bf16 activations (fp16 MMA), fp32 accumulate",
         "data": "synthetic (seeded random weights and activations of the stated shapes)", "config": config,
+        "weight_layout": args.layout,
         "us_per_round": {str(k): round(v, 2) for k, v in sorted(us.items())},
         "weight_stream_gbs": {str(k): round(v, 1) for k, v in sorted(gbs.items())},
         "pct_of_measured_hbm": {str(k): round(100 * v / hbm, 1) for k, v in sorted(gbs.items())},
