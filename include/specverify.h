@@ -278,7 +278,9 @@ size_t sv_round_workspace_bytes(const sv_model* model, int rows);
  * use it.  sv_qmm_pack_bytes returns ceil(N/64)*64 * K * (bits/8 + 4/64)
  * bytes, or 0 for unsupported sizes (K a multiple of 512).  sv_qmm_pack
  * validates like sv_qmm_verify, launches one kernel on `stream`, and writes
- * only `packed` (caller-owned device memory, 16-byte aligned). */
+ * only `packed` (caller-owned device memory, 16-byte aligned).  The pages
+ * have no counterpart: their weights are used in the canonical layout, and
+ * this copy only changes where the same bytes sit. */
 size_t sv_qmm_pack_bytes(int N, int K, int bits);
 int sv_qmm_pack(const uint32_t* wq, const uint16_t* scales, const uint16_t* biases, int N, int K, int bits, int group,
                 void* packed, size_t packed_bytes, void* stream);
