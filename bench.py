@@ -288,7 +288,7 @@ def cpu_cores():
 
 # -------------------------------------------------------- ncu DRAM traffic
 # DRAM bytes (read + write) per launch of the persistent kernel, from one ncu
-# capture of a smaller round (profiles/stream_kernel_m8_4layers.md), scaled to
+# capture of a smaller round (4 layers, M = 8), scaled to
 # a full launch by weight bytes; valid only for the kernel source it was taken
 # on, so the source's hash is checked and the figure dropped when it differs.
 TRAFFIC_CAPTURE = {"sha256": "0f292be305e8bd4d84ab514826071a6eedc221f1a39c5abd086ee7d7e9034684", "M": 8,
@@ -361,7 +361,7 @@ def main():
     import __graft_entry__
     __graft_entry__.build()
     from speculative_decoding_verify_qmm_gb300 import binding
-    from tests import _model
+    from synthetic import model as _model
     import synthetic
     lib = binding.load()
 

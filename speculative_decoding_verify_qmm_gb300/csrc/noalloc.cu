@@ -9,8 +9,6 @@
 // activations and the split-K partials) in one file-scope device array of
 // fixed size.  Every GPU that loads this library holds that array until the
 // process exits.
-#include <mutex>
-
 #include "sv_internal.h"
 
 namespace sv {
@@ -20,23 +18,15 @@ constexpr size_t NOALLOC_SCRATCH_BYTES = size_t(4) << 20;  // 4 MiB
 static __device__ __align__(256) uint8_t g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
 
 // Device address of the array on the current device.  In host code the
-// array's name is only a host-side stand-in, so the address is looked up once
-// per device (with that device current) and cached.
+// array's name is only a host-side stand-in, so the address is looked up on
+// every call, with the calling thread's current device: once the module is
+// loaded this is a cheap table lookup, and it stays right if the context was
+// torn down and rebuilt (cudaDeviceReset) since the previous call.
 static int noalloc_scratch(void** out) {
-  static std::mutex mu;
-  static void* cache[64] = {nullptr};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  if (dev < 0 || dev >= 64) return fail(SV_EUNSUPPORTED, "device ordinal %d out of range", dev);
-  std::lock_guard<std::mutex> lock(mu);
-  if (!cache[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
-    cache[dev] = p;
-  }
-  *out = cache[dev];
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
+  *out = p;
   return SV_OK;
 }
 

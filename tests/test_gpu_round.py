@@ -6,7 +6,7 @@ import torch
 
 from oracle import accept as oa, chain, glue, qmm as oq, quant
 import synthetic
-from tests import _model
+from synthetic import model as _model
 from tests._util import assert_close_bf16, assert_close_rms, dev_bf16, host_bf16_bits, host_f32_of_bf16, sub_weight
 
 pytestmark = pytest.mark.gpu
