@@ -96,8 +96,13 @@ int sv_qmm_verify(const uint32_t* wq, const uint16_t* scales, const uint16_t* bi
  * exits.  Calls whose scratch would exceed it (roughly M = 32 with K above
  * 20k) return SV_EUNSUPPORTED with the needed size in sv_last_error().
  * Same arguments and results as sv_qmm_verify, minus the workspace.
- *   - The first call on a device looks up the array's device address; make
- *     that first call before any stream capture.
+ *   - The array and this library's kernels get their device memory when
+ *     CUDA loads the library's module on a device, which with CUDA's default
+ *     lazy loading happens at the first call there: make one call per
+ *     device at start-up, outside any no-allocation window and before any
+ *     stream capture.  Every call looks the array's device address up again
+ *     (cheap once loaded), so a context rebuilt after cudaDeviceReset is
+ *     handled.
  *   - Every call shares the array and clears its own counters first; calls
  *     that overlap on the GPU (other streams, or other host threads) race on
  *     the array, so order them on one stream.
@@ -301,6 +306,56 @@ int sv_verify_round(const sv_model* model, const void* plan, int B, const int32_
                     float temperature, const float* q, int ldq, const int32_t* draft, const float* u, float* logits,
                     int ldl, int32_t* out_len, int32_t* out_tokens, void* workspace, size_t workspace_bytes,
                     void* stream, void* event_start, void* event_stop);
+
+/* ------------------------------------------------------- draft-cap control ---
+ * Host-only (no device work, callable without a GPU).  PyPI page, "The
+ * Apple-Silicon speedup ceiling": throughput is about A / (drafter + overhead
+ * + verify cost) for accept length A and draft cap C, with the verify cost of
+ * a wider round measured rather than assumed; wiki page, "Key techniques"
+ * (hardware-aware auto-calibration): a controller picks each round's cap from
+ * the measured curves and a live acceptance estimate, with expected committed
+ * tokens 1 + sum_{i=1}^{C} p^i, and parks speculation (cap 0) when it loses;
+ * PyPI page, "Tuning" (--max-draft auto): while parked, plain steps plus
+ * periodic probe rounds keep the estimate current.
+ *   verify_us[C]  measured device time of a verify round of width M = 1 + C
+ *                 (e.g. sv_verify_round timed at every M), C = 0..max_cap, > 0;
+ *   draft_us[C]   the drafter's cost of a block of C drafts (draft_us[0] is
+ *                 normally 0), >= 0;  overhead_us  per-round host overhead.
+ * A round's cost is draft_us[C] + overhead_us + verify_us[C]; the best cap
+ * maximises E(C) / cost(C), E(C) = sum_{i=0}^{C} p^i, smallest C on ties.
+ * The acceptance estimate p = S / (S + F), where a round that verified C
+ * drafts and accepted a adds a to S and [a < C] to F through an EWMA of
+ * weight alpha (the maximum-likelihood estimate of a geometric acceptance
+ * model); the prior p0 counts as one round.  The struct is caller-owned; its
+ * state fields are written by the calls below.  Errors: SV_EINVAL. */
+#define SV_CAP_MAX 31
+typedef struct {
+  int max_cap;                        /* 0..SV_CAP_MAX */
+  double verify_us[SV_CAP_MAX + 1];
+  double draft_us[SV_CAP_MAX + 1];
+  double overhead_us;
+  double alpha;                       /* EWMA weight of the newest round, (0, 1] */
+  int probe_every;                    /* while parked: one probe round every probe_every rounds */
+  int probe_cap;                      /* cap of a probe round, 1..max_cap */
+  double S, F;                        /* state: EWMA successes and failures */
+  int parked, since_probe;            /* state */
+} sv_cap_controller;
+/* 1 + p + ... + p^cap (NAN for p outside [0, 1] or cap < 0). */
+double sv_expected_committed(double p, int cap);
+/* The best cap for a given p and its rate (committed tokens per microsecond). */
+int sv_best_cap(double p, int max_cap, const double* verify_us, const double* draft_us, double overhead_us, int* cap,
+                double* rate);
+/* End of the cheap verify region (PyPI page, "Results at a glance"): the widest
+ * M such that verify_us[c] <= (1 + tol) * verify_us[0] for every c < M. */
+int sv_verify_knee(const double* verify_us, int n, double tol, int* width);
+int sv_cap_init(sv_cap_controller* ctl, int max_cap, const double* verify_us, const double* draft_us,
+                double overhead_us, double alpha, int probe_every, int probe_cap, double p0);
+/* Cap for the next round (0 = a plain step). */
+int sv_cap_next(sv_cap_controller* ctl, int* cap);
+/* Record a round that verified `cap` drafts and accepted `accepted` of them. */
+int sv_cap_update(sv_cap_controller* ctl, int cap, int accepted);
+/* The current acceptance estimate S / (S + F). */
+double sv_cap_acceptance(const sv_cap_controller* ctl);
 
 #ifdef __cplusplus
 }

@@ -25,10 +25,13 @@ printed on the source pages):
   drive sampled acceptance.
 * ``glue``   - RMSNorm, residual add and SwiGLU between projections.
 * ``chain``  - one verify round of a dense decoder stack built from the above.
+* ``cap``    - the draft-cap choice from measured verify costs and a live
+  acceptance estimate (PyPI page, "The Apple-Silicon speedup ceiling";
+  wiki page, "Key techniques").
 
 Floating point is fp64 unless a step fixes another precision; every place
 where the pages are silent and a plain reading was taken is marked
 "[reading]".
 """
 
-from . import quant, qmm, accept, philox, glue, chain  # noqa: F401
+from . import quant, qmm, accept, philox, glue, chain, cap  # noqa: F401

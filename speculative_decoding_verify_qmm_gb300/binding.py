@@ -44,6 +44,22 @@ class Model(ctypes.Structure):
 
 _c_model_p = ctypes.POINTER(Model)
 
+SV_CAP_MAX = 31
+
+
+class CapState(ctypes.Structure):
+    """sv_cap_controller (host memory)."""
+    _fields_ = [("max_cap", ctypes.c_int), ("verify_us", ctypes.c_double * (SV_CAP_MAX + 1)),
+                ("draft_us", ctypes.c_double * (SV_CAP_MAX + 1)), ("overhead_us", ctypes.c_double),
+                ("alpha", ctypes.c_double), ("probe_every", ctypes.c_int), ("probe_cap", ctypes.c_int),
+                ("S", ctypes.c_double), ("F", ctypes.c_double), ("parked", ctypes.c_int),
+                ("since_probe", ctypes.c_int)]
+
+
+_c_cap_p = ctypes.POINTER(CapState)
+_c_f64_p = ctypes.POINTER(ctypes.c_double)
+_c_int_p = ctypes.POINTER(ctypes.c_int)
+
 _SIGNATURES = {
     "sv_status_string": (ctypes.c_char_p, [_c_int]),
     "sv_last_error": (ctypes.c_char_p, []),
@@ -86,7 +102,67 @@ _SIGNATURES = {
     "sv_rmsnorm": (_c_int, [_c_void_p, _c_int, _c_int, _c_int, _c_void_p, _c_float, _c_void_p, _c_int, _c_void_p]),
     "sv_residual_add": (_c_int, [_c_void_p, _c_int, _c_void_p, _c_int, _c_int, _c_int, _c_void_p]),
     "sv_swiglu": (_c_int, [_c_void_p, _c_int, _c_void_p, _c_int, _c_int, _c_int, _c_void_p, _c_int, _c_void_p]),
+    "sv_expected_committed": (ctypes.c_double, [ctypes.c_double, _c_int]),
+    "sv_best_cap": (_c_int, [ctypes.c_double, _c_int, _c_f64_p, _c_f64_p, ctypes.c_double, _c_int_p, _c_f64_p]),
+    "sv_verify_knee": (_c_int, [_c_f64_p, _c_int, ctypes.c_double, _c_int_p]),
+    "sv_cap_init": (_c_int, [_c_cap_p, _c_int, _c_f64_p, _c_f64_p, ctypes.c_double, ctypes.c_double, _c_int, _c_int,
+                             ctypes.c_double]),
+    "sv_cap_next": (_c_int, [_c_cap_p, _c_int_p]),
+    "sv_cap_update": (_c_int, [_c_cap_p, _c_int, _c_int]),
+    "sv_cap_acceptance": (ctypes.c_double, [_c_cap_p]),
 }
+
+
+def _f64_array(values):
+    arr = (ctypes.c_double * len(values))(*[float(v) for v in values])
+    return ctypes.cast(arr, _c_f64_p), arr
+
+
+class CapController:
+    """sv_cap_controller: per-round draft cap from measured costs (host only)."""
+
+    def __init__(self, lib, max_cap, verify_us, draft_us, overhead_us, alpha, probe_every, probe_cap, p0):
+        self.lib, self.state = lib, CapState()
+        v, self._v = _f64_array(verify_us)
+        d, self._d = _f64_array(draft_us)
+        _check(lib, lib.sv_cap_init(ctypes.byref(self.state), max_cap, v, d, overhead_us, alpha, probe_every,
+                                    probe_cap, p0))
+
+    def next_cap(self):
+        c = ctypes.c_int()
+        _check(self.lib, self.lib.sv_cap_next(ctypes.byref(self.state), ctypes.byref(c)))
+        return c.value
+
+    def update(self, cap, accepted):
+        _check(self.lib, self.lib.sv_cap_update(ctypes.byref(self.state), cap, accepted))
+
+    def p(self):
+        return self.lib.sv_cap_acceptance(ctypes.byref(self.state))
+
+    @property
+    def parked(self):
+        return bool(self.state.parked)
+
+
+def best_cap(lib, p, verify_us, draft_us, overhead_us):
+    """(cap, rate) from sv_best_cap; max_cap = len(verify_us) - 1."""
+    v, _v = _f64_array(verify_us)
+    d, _d = _f64_array(draft_us)
+    c, r = ctypes.c_int(), ctypes.c_double()
+    _check(lib, lib.sv_best_cap(p, len(verify_us) - 1, v, d, overhead_us, ctypes.byref(c), ctypes.byref(r)))
+    return c.value, r.value
+
+
+def verify_knee(lib, verify_us, tol):
+    v, _v = _f64_array(verify_us)
+    w = ctypes.c_int()
+    _check(lib, lib.sv_verify_knee(v, len(verify_us), tol, ctypes.byref(w)))
+    return w.value
+
+
+def _check(lib, status):
+    if status != SV_OK:
+        raise SVError(status, lib.sv_last_error().decode())
 
 
 class SVError(RuntimeError):
