@@ -140,3 +140,110 @@ def spec_accept_batched(logits, q, drafts, row_offsets, temperature, us):
         out.append(spec_accept(np.asarray(logits)[r0:r1], q_b, drafts[b], temperature,
                                None if us is None else us[b]))
     return out
+
+
+# ------------------------------------------------------------- truncation
+# mlx-dspark releases page, v0.1.0 "Highlights": lossless top-p / top-k -
+# nucleus / top-k truncation applied to both the draft and the target, so
+# sampling stays an exact sample from the truncated target.  Readings taken:
+#
+# * The order is by the row's own values, largest first, ties to the lower
+#   index: by the fp32 logit for the target (probabilities are monotone in it),
+#   by the fp32 probability for a draft row.
+# * top_k > 0 keeps the first top_k tokens in that order (0 = no limit).
+# * top_p < 1 then keeps, among those, the shortest prefix whose probability
+#   (renormalised over the top_k survivors) reaches top_p (1 = no limit).
+# * The kept weights are renormalised; everything else gets probability 0.
+# * The draft's truncation is the draft sampler's business (the library offers
+#   the same rule for probability rows); the accept step truncates the target
+#   and uses q as given, the distribution the drafts were drawn from.
+
+def truncation_mask(keys, weights, top_k, top_p):
+    """Boolean kept-mask of one row: order by keys (desc, ties to lower index),
+    keep the first top_k, then the shortest prefix of those whose weight share
+    reaches top_p."""
+    keys = np.asarray(keys)
+    w = np.asarray(weights, dtype=np.float64)
+    V = keys.shape[0]
+    order = np.lexsort((np.arange(V), -keys.astype(np.float64)))   # keys desc, then index asc
+    n = V if top_k <= 0 else min(top_k, V)
+    if top_p < 1.0:
+        c = np.cumsum(w[order[:n]])
+        total = c[-1]
+        reach = np.nonzero(c >= top_p * total)[0]
+        n = int(reach[0]) + 1 if reach.size else n
+    mask = np.zeros(V, dtype=bool)
+    mask[order[:n]] = True
+    return mask
+
+
+def truncated_target_probs(logits_row, temperature, top_k, top_p):
+    """p' of one target row: softmax(z / T) restricted to the kept set, renormalised (fp64)."""
+    z = np.asarray(logits_row, dtype=np.float32)
+    e = np.exp((z.astype(np.float64) - float(z.max())) / float(temperature))
+    keep = truncation_mask(z, e, top_k, top_p)
+    e = np.where(keep, e, 0.0)
+    return e / e.sum()
+
+
+def truncate_probs(q_row, top_k, top_p):
+    """The same rule on a probability row (fp32 in, fp64 out), for the draft side."""
+    q = np.asarray(q_row, dtype=np.float32)
+    w = q.astype(np.float64)
+    keep = truncation_mask(q, w, top_k, top_p)
+    w = np.where(keep, w, 0.0)
+    return w / w.sum()
+
+
+def sampled_accept_truncated_detail(logits, q, draft, temperature, u, top_k, top_p):
+    """sampled_accept_detail with the target truncated (top_k / top_p) in every row."""
+    if not temperature > 0:
+        raise ValueError("sampled accept needs T > 0")
+    z = np.asarray(logits, dtype=np.float32)
+    qf = np.asarray(q, dtype=np.float32)
+    draft = [int(d) for d in draft]
+    u = np.asarray(u, dtype=np.float32)
+    m = len(draft)
+    tokens, ratios = [], []
+    for i in range(m):
+        p_i = truncated_target_probs(z[i], temperature, top_k, top_p)
+        q_i = qf[i].astype(np.float64)
+        d = draft[i]
+        # a token the truncated target never emits is rejected whatever q says
+        r = 0.0 if p_i[d] == 0.0 else (np.inf if q_i[d] == 0.0 else p_i[d] / q_i[d])
+        ratios.append(r)
+        if float(u[i]) < r:
+            tokens.append(d)
+            continue
+        residual = np.maximum(0.0, p_i - q_i)
+        kind = "residual"
+        if residual.sum() == 0.0:
+            residual, kind = p_i, "p_fallback"
+        k, theta, c = inverse_cdf(residual, u[m])
+        tokens.append(k)
+        return dict(out_len=len(tokens), tokens=tokens, ratios=ratios, reject=i,
+                    weights_kind=kind, theta=theta, Z=float(c[-1]), cdf=c)
+    p_m = truncated_target_probs(z[m], temperature, top_k, top_p)
+    k, theta, c = inverse_cdf(p_m, u[m])
+    tokens.append(k)
+    return dict(out_len=len(tokens), tokens=tokens, ratios=ratios, reject=-1,
+                weights_kind="bonus", theta=theta, Z=float(c[-1]), cdf=c)
+
+
+# ---------------------------------------------------------------- logprobs
+# mlx-dspark releases page, v0.2.0 "Highlights": logprobs / top_logprobs, the
+# chosen and the top-k target log-probabilities per token.  [reading] At
+# temperature T (T = 1 when the round is greedy): log p_v = (z_v - max) / T -
+# log sum_k exp((z_k - max) / T); the top list is ordered like truncation
+# (logit desc, ties to the lower index).
+
+def logprobs(logits_row, temperature, chosen, top_n):
+    """(log p[chosen], top ids, top log-probabilities) of one row, fp64."""
+    z = np.asarray(logits_row, dtype=np.float32)
+    T = float(temperature) if temperature > 0 else 1.0
+    d = (z.astype(np.float64) - float(z.max())) / T
+    lse = np.log(np.exp(d).sum())
+    lp = d - lse
+    V = z.shape[0]
+    order = np.lexsort((np.arange(V), -z.astype(np.float64)))[:top_n]
+    return float(lp[int(chosen)]), order.astype(np.int64), lp[order]

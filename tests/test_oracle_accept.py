@@ -153,3 +153,89 @@ def test_batched_equals_per_request():
         want = accept.sampled_accept(z[offs[b]:offs[b + 1]], q[qo:qo + mm], drafts[b], T, us[b])
         qo += mm
         assert got[b] == want
+
+
+# ----------------------------------------------------- truncation and logprobs
+
+def test_truncation_hand_examples():
+    w = np.array([0.1, 0.5, 0.1, 0.3])
+    keys = w.astype(np.float32)
+    assert list(accept.truncation_mask(keys, w, 0, 0.8)) == [False, True, False, True]      # 0.5 + 0.3 reaches 0.8
+    assert list(accept.truncation_mask(keys, w, 0, 0.81)) == [True, True, False, True]      # the tie goes to index 0
+    assert list(accept.truncation_mask(keys, w, 1, 1.0)) == [False, True, False, False]
+    assert list(accept.truncation_mask(keys, w, 3, 1.0)) == [True, True, False, True]
+    # top_k first, then top_p over the renormalised survivors: (0.5, 0.3) -> shares (0.625, 0.375)
+    assert list(accept.truncation_mask(keys, w, 2, 0.6)) == [False, True, False, False]
+    assert list(accept.truncation_mask(keys, w, 2, 0.7)) == [False, True, False, True]
+    flat = np.full(6, 1 / 6)
+    assert list(accept.truncation_mask(flat.astype(np.float32), flat, 2, 1.0)) == [True, True, False, False, False, False]
+
+
+def test_no_truncation_is_the_plain_target():
+    r = synthetic.rng(60)
+    z = (r.standard_normal(50) * 2).astype(np.float32)
+    assert np.allclose(accept.truncated_target_probs(z, 0.8, 0, 1.0), qmm.target_probs(z, 0.8), rtol=1e-12)
+    assert np.allclose(accept.truncated_target_probs(z, 0.8, 50, 1.0), qmm.target_probs(z, 0.8), rtol=1e-12)
+
+
+def test_top_k_one_sampled_accept_is_greedy():
+    # the truncated target is one-hot on the argmax: sampled acceptance reduces to greedy
+    r = synthetic.rng(61)
+    for _ in range(200):
+        V, m = 20, int(r.integers(0, 6))
+        z = (r.standard_normal((m + 1, V)) * 2).astype(np.float32)
+        am = np.argmax(z, axis=1)
+        draft = [int(am[i]) if r.random() < 0.6 else int(r.integers(0, V)) for i in range(m)]
+        q = scipy.special.softmax(r.standard_normal((m, V)), axis=1).astype(np.float32)
+        u = r.random(m + 1).astype(np.float32)
+        d = accept.sampled_accept_truncated_detail(z, q, draft, 1.0, u, 1, 1.0)
+        assert (d["out_len"], d["tokens"]) == accept.greedy_accept(z, draft)
+
+
+def test_truncated_sampled_accept_follows_truncated_target_chi_square():
+    r = synthetic.rng(62)
+    V, T, m, rounds, top_k, top_p = 16, 1.0, 2, 60_000, 10, 0.8
+    z = (r.standard_normal((m + 1, V)) * 1.2).astype(np.float32)
+    q = scipy.special.softmax(z[:m].astype(np.float64) + r.standard_normal((m, V)), axis=1).astype(np.float32)
+    p0 = accept.truncated_target_probs(z[0], T, top_k, top_p)
+    p1 = accept.truncated_target_probs(z[1], T, top_k, top_p)
+    assert (p0 == 0).sum() >= 6                       # the truncation does remove tokens
+    qc = [np.cumsum(q[i].astype(np.float64) / q[i].astype(np.float64).sum()) for i in range(m)]
+    first, second = np.zeros(V), np.zeros(V)
+    for _ in range(rounds):
+        draft = [min(int(np.searchsorted(qc[i], r.random(), side="right")), V - 1) for i in range(m)]
+        u = r.random(m + 1).astype(np.float32)
+        d = accept.sampled_accept_truncated_detail(z, q, draft, T, u, top_k, top_p)
+        first[d["tokens"][0]] += 1
+        if d["out_len"] >= 2:
+            second[d["tokens"][1]] += 1
+    assert first[p0 == 0].sum() == 0 and second[p1 == 0].sum() == 0   # never outside the kept set
+    keep0, keep1 = p0 > 0, p1 > 0
+    assert _chi2_pvalue(first[keep0], p0[keep0]) > 1e-3
+    assert _chi2_pvalue(second[keep1], p1[keep1]) > 1e-3
+    # the pin can fail: the untruncated target is rejected
+    full = qmm.target_probs(z[0], T)
+    assert _chi2_pvalue(first, full) < 1e-3
+
+
+def test_truncate_probs_rule():
+    q = np.array([0.05, 0.4, 0.05, 0.3, 0.2], np.float32)
+    out = accept.truncate_probs(q, 0, 0.85)                # 0.4 + 0.3 + 0.2 = 0.9 >= 0.85
+    assert np.allclose(out, [0, 0.4 / 0.9, 0, 0.3 / 0.9, 0.2 / 0.9])
+    out = accept.truncate_probs(q, 2, 1.0)
+    assert np.allclose(out, [0, 0.4 / 0.7, 0, 0.3 / 0.7, 0])
+
+
+def test_logprobs_closed_forms():
+    V = 10
+    lp, ids, top = accept.logprobs(np.zeros(V, np.float32), 1.0, 3, 4)
+    assert lp == pytest.approx(-np.log(V)) and list(ids) == [0, 1, 2, 3]
+    assert np.allclose(top, -np.log(V))
+    r = synthetic.rng(63)
+    z = (r.standard_normal(300) * 3).astype(np.float32)
+    for T in (0.0, 0.7, 1.0):
+        want = scipy.special.log_softmax(z.astype(np.float64) / (T if T > 0 else 1.0))
+        lp, ids, top = accept.logprobs(z, T, 17, 5)
+        assert lp == pytest.approx(want[17], rel=1e-12)
+        assert list(ids) == list(np.argsort(-want, kind="stable")[:5])
+        assert np.allclose(top, want[ids], rtol=1e-12)
