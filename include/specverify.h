@@ -190,6 +190,41 @@ int sv_spec_accept_batched(int B, const int32_t* row_offsets, const float* logit
                            const int32_t* draft, int V, float temperature, const float* u, int32_t* out_len,
                            int32_t* out_tokens, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Accept with a truncated target (releases page, v0.1.0 "Highlights":
+ * lossless top-p / top-k, the truncation applied to both the draft and the
+ * target so the output is an exact sample of the truncated target).  As
+ * sv_spec_accept_batched, except that for T > 0 every logits row's target
+ * p = softmax(z / T) is first truncated: tokens are ordered by logit, largest
+ * first, ties to the lower index; top_k > 0 keeps the first top_k (0 = no
+ * limit), then top_p keeps the shortest prefix of those whose share of their
+ * mass reaches top_p (1 = no limit); the kept mass is renormalised and every
+ * other token has probability 0.  A draft token outside the kept set is
+ * rejected.  q must be the distribution the drafts were actually drawn from
+ * (truncate it with sv_truncate_probs to apply the same rule on the draft
+ * side).  Greedy rounds (T == 0) are unaffected: the argmax is always kept.
+ * top_k >= 0, 0 < top_p <= 1.  Workspace: sv_accept_workspace_bytes(). */
+int sv_spec_accept_truncated(int B, const int32_t* row_offsets, const float* logits, int ldl, const float* row_max,
+                             const float* row_sumexp, const int32_t* row_argmax, const float* q, int ldq,
+                             const int32_t* draft, int V, float temperature, const float* u, int top_k, float top_p,
+                             int32_t* out_len, int32_t* out_tokens, void* workspace, size_t workspace_bytes,
+                             void* stream);
+/* The same truncation rule on probability rows (the draft side): each row of
+ * probs fp32 [rows, V] (stride ldp) is ordered by value (ties to the lower
+ * index), truncated by top_k / top_p and renormalised into out (stride ldo;
+ * out may equal probs, otherwise it must not overlap it).  No workspace. */
+int sv_truncate_probs(const float* probs, int ldp, float* out, int ldo, int rows, int V, int top_k, float top_p,
+                      void* stream);
+/* Log-probabilities of the target (releases page, v0.2.0 "Highlights":
+ * logprobs / top_logprobs, the chosen and the top target log-probabilities
+ * per token).  Per row of logits fp32 [rows, V] (stride ldl), at temperature T
+ * (T == 0: T = 1): log p_v = (z_v - max) / T - log sum_k exp((z_k - max) / T),
+ * in fp64, stored fp32.  chosen int32 [rows] (may be NULL) -> chosen_logprob
+ * fp32 [rows] (NaN for an index outside [0, V)); top_n in [0, 32] -> top_ids
+ * int32 [rows, top_n] and top_logprobs fp32 [rows, top_n], ordered by logit
+ * (largest first, ties to the lower index).  No workspace. */
+int sv_logprobs(const float* logits, int ldl, int rows, int V, float temperature, const int32_t* chosen, int top_n,
+                float* chosen_logprob, int32_t* top_ids, float* top_logprobs, void* stream);
+
 /* --------------------------------------------------------------- philox ---
  * n uniforms in [0, 1) from Philox-4x32-10 (Salmon et al., SC'11): element i is
  * word (offset+i) % 4 of Philox(counter = (b lo, b hi, subsequence lo,

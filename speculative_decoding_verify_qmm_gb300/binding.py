@@ -102,6 +102,13 @@ _SIGNATURES = {
     "sv_rmsnorm": (_c_int, [_c_void_p, _c_int, _c_int, _c_int, _c_void_p, _c_float, _c_void_p, _c_int, _c_void_p]),
     "sv_residual_add": (_c_int, [_c_void_p, _c_int, _c_void_p, _c_int, _c_int, _c_int, _c_void_p]),
     "sv_swiglu": (_c_int, [_c_void_p, _c_int, _c_void_p, _c_int, _c_int, _c_int, _c_void_p, _c_int, _c_void_p]),
+    "sv_spec_accept_truncated": (_c_int, [_c_int, _c_i32_p, _c_void_p, _c_int, _c_void_p, _c_void_p, _c_void_p,
+                                          _c_void_p, _c_int, _c_void_p, _c_int, _c_float, _c_void_p, _c_int,
+                                          _c_float, _c_void_p, _c_void_p, _c_void_p, _c_size_t, _c_void_p]),
+    "sv_truncate_probs": (_c_int, [_c_void_p, _c_int, _c_void_p, _c_int, _c_int, _c_int, _c_int, _c_float,
+                                   _c_void_p]),
+    "sv_logprobs": (_c_int, [_c_void_p, _c_int, _c_int, _c_int, _c_float, _c_void_p, _c_int, _c_void_p, _c_void_p,
+                             _c_void_p, _c_void_p]),
     "sv_expected_committed": (ctypes.c_double, [ctypes.c_double, _c_int]),
     "sv_best_cap": (_c_int, [ctypes.c_double, _c_int, _c_f64_p, _c_f64_p, ctypes.c_double, _c_int_p, _c_f64_p]),
     "sv_verify_knee": (_c_int, [_c_f64_p, _c_int, ctypes.c_double, _c_int_p]),
@@ -399,6 +406,47 @@ class Library:
             q.stride(0) if q is not None else 0, _ptr(drafts), V, float(temperature), _ptr(u), _ptr(out_len),
             _ptr(out_tokens), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
         return out_len, out_tokens
+
+    def spec_accept_truncated(self, row_offsets, logits, drafts, temperature, top_k, top_p, q=None, u=None,
+                              stats=None, workspace=None, stream=None):
+        import torch
+        B = len(row_offsets) - 1
+        rows = int(row_offsets[-1])
+        V = logits.shape[1]
+        dev = logits.device
+        offs = (ctypes.c_int32 * (B + 1))(*[int(v) for v in row_offsets])
+        out_len = torch.zeros(B, dtype=torch.int32, device=dev)
+        out_tokens = torch.full((rows,), -1, dtype=torch.int32, device=dev)
+        if workspace is None:
+            workspace = self.workspace(self.accept_workspace_bytes(B, rows), dev)
+        rmax, rsum, rarg = stats if stats is not None else (None, None, None)
+        self.check(self.lib.sv_spec_accept_truncated(
+            B, offs, _ptr(logits), logits.stride(0), _ptr(rmax), _ptr(rsum), _ptr(rarg), _ptr(q),
+            q.stride(0) if q is not None else 0, _ptr(drafts), V, float(temperature), _ptr(u), int(top_k),
+            float(top_p), _ptr(out_len), _ptr(out_tokens), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _stream(stream)))
+        return out_len, out_tokens
+
+    def truncate_probs(self, probs, top_k, top_p, out=None, stream=None):
+        import torch
+        if out is None:
+            out = torch.empty_like(probs)
+        self.check(self.lib.sv_truncate_probs(_ptr(probs), probs.stride(0), _ptr(out), out.stride(0), probs.shape[0],
+                                              probs.shape[1], int(top_k), float(top_p), _stream(stream)))
+        return out
+
+    def logprobs(self, logits, temperature, chosen=None, top_n=0, stream=None):
+        """(chosen_logprob [rows] or None, top_ids [rows, top_n], top_logprobs [rows, top_n])."""
+        import torch
+        rows, V = logits.shape
+        dev = logits.device
+        clp = torch.empty(rows, dtype=torch.float32, device=dev) if chosen is not None else None
+        ids = torch.empty((rows, top_n), dtype=torch.int32, device=dev)
+        tlp = torch.empty((rows, top_n), dtype=torch.float32, device=dev)
+        self.check(self.lib.sv_logprobs(_ptr(logits), logits.stride(0), rows, V, float(temperature), _ptr(chosen),
+                                        int(top_n), _ptr(clp), _ptr(ids) if top_n else None,
+                                        _ptr(tlp) if top_n else None, _stream(stream)))
+        return clp, ids, tlp
 
     # --------------------------------------------------------------- philox
     def philox_uniforms(self, seed, subsequence, offset, n, out=None, stream=None):

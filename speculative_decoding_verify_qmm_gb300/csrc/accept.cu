@@ -89,9 +89,17 @@ __global__ void __launch_bounds__(ACC_THREADS) accept_kernel(const AcceptParams 
         // fp32 ratio (relative error a few 1e-7); fp64 only when u is near it
         const float qd = p.q[(size_t)(qd0 + tid) * p.ldq + d];
         const float z = p.logits[(size_t)(r0 + tid) * p.ldl + d];
-        const float zmx = p.row_max[r0 + tid], se = p.row_sumexp[r0 + tid], ui = p.u[r0 + tid];
-        const float r32 = qd == 0.f ? INFINITY : expf((z - zmx) / p.temperature) / se / qd;
-        if (fabsf(ui - r32) > 1e-5f * fmaxf(1.f, r32)) {
+        const float zmx = p.row_max[r0 + tid], ui = p.u[r0 + tid];
+        const float se = p.tkey ? p.tnorm[r0 + tid] : p.row_sumexp[r0 + tid];
+        bool kept = true;  // a token the truncated target never emits is rejected
+        if (p.tkey) {
+          const uint32_t kd = order_key(z), K = p.tkey[r0 + tid];
+          kept = kd > K || (kd == K && d <= p.tidx[r0 + tid]);
+        }
+        const float r32 = !kept ? 0.f : (qd == 0.f ? INFINITY : expf((z - zmx) / p.temperature) / se / qd);
+        if (!kept) {
+          rej = true;
+        } else if (fabsf(ui - r32) > 1e-5f * fmaxf(1.f, r32)) {
           rej = !(ui < r32);
         } else {
           const double pd = exp(((double)z - (double)zmx) / (double)p.temperature) / (double)se;
@@ -108,9 +116,18 @@ __global__ void __launch_bounds__(ACC_THREADS) accept_kernel(const AcceptParams 
   const int row = r0 + j;
   const float* z = p.logits + (size_t)row * p.ldl;
   const float* qr = resid ? p.q + (size_t)(qd0 + j) * p.ldq : nullptr;
-  const float zmax = p.row_max[row], S = p.row_sumexp[row], T = p.temperature;
+  const bool trunc = p.tkey != nullptr;
+  const float zmax = p.row_max[row], S = trunc ? p.tnorm[row] : p.row_sumexp[row], T = p.temperature;
+  const uint32_t tK = trunc ? p.tkey[row] : 0u;
+  const int tI = trunc ? p.tidx[row] : V;
   auto weight = [&](int k, float& pk) -> float {
-    pk = expf((z[k] - zmax) / T) / S;
+    const float zk = z[k];
+    bool kept = true;
+    if (trunc) {
+      const uint32_t key = order_key(zk);
+      kept = key > tK || (key == tK && k <= tI);
+    }
+    pk = kept ? expf((zk - zmax) / T) / S : 0.f;
     return resid ? fmaxf(0.f, pk - qr[k]) : pk;
   };
 

@@ -446,12 +446,14 @@ static int accept_chunks(int V) {
 // statistics) the statistics of every row.
 static size_t accept_sums_offset() { return COUNTER_BYTES; }
 static size_t accept_stats_offset(int B) { return COUNTER_BYTES + align256((size_t)B * 64 * 2 * 8); }
-size_t accept_bytes(int B, int rows) { return accept_stats_offset(B) + align256((size_t)rows * 12); }
+// per logits row: truncation key, tie index and kept mass of the target
+static size_t accept_trunc_offset(int B, int rows) { return accept_stats_offset(B) + align256((size_t)rows * 12); }
+size_t accept_bytes(int B, int rows) { return accept_trunc_offset(B, rows) + align256((size_t)rows * 12); }
 
 int accept_internal(int B, const int32_t* offs, const float* logits, int ldl, const float* row_max,
                     const float* row_sumexp, const int32_t* row_argmax, const float* q, int ldq, const int32_t* draft,
                     int V, float temperature, const float* u, int32_t* out_len, int32_t* out_tokens, void* ws,
-                    cudaStream_t s) {
+                    cudaStream_t s, int top_k, float top_p) {
   uint8_t* base = static_cast<uint8_t*>(ws);
   const int rows = offs[B];
   AcceptParams p;
@@ -472,6 +474,28 @@ int accept_internal(int B, const int32_t* offs, const float* logits, int ldl, co
     p.row_max = row_max;
     p.row_sumexp = row_sumexp;
     p.row_argmax = row_argmax;
+  }
+  if (temperature > 0.f && ((top_k > 0 && top_k < V) || top_p < 1.f)) {
+    // truncation bounds of every row's target before the accept decisions
+    uint8_t* tb = base + accept_trunc_offset(B, rows);
+    SelectArgs a;
+    memset(&a, 0, sizeof(a));
+    a.x = logits;
+    a.ldx = ldl;
+    a.V = V;
+    a.mode = SEL_LOGITS;
+    a.row_max = p.row_max;
+    a.temperature = temperature;
+    a.top_k = top_k;
+    a.top_p = top_p;
+    a.out_key = reinterpret_cast<uint32_t*>(tb);
+    a.out_idx = reinterpret_cast<int32_t*>(tb + 4 * (size_t)rows);
+    a.out_norm = reinterpret_cast<float*>(tb + 8 * (size_t)rows);
+    cudaError_t e = launch_select(a, rows, s);
+    if (e != cudaSuccess) return cuda_fail(e, "truncation launch");
+    p.tkey = a.out_key;
+    p.tidx = a.out_idx;
+    p.tnorm = a.out_norm;
   }
   p.q = q;
   p.ldq = ldq;
@@ -536,7 +560,83 @@ int sv_spec_accept_batched(int B, const int32_t* row_offsets, const float* logit
   const size_t need = accept_bytes(B, row_offsets[B]);
   if (workspace_bytes < need) return fail(SV_EINVAL, "workspace too small: %zu < %zu", workspace_bytes, need);
   return accept_internal(B, row_offsets, logits, ldl, row_max, row_sumexp, row_argmax, q, ldq, draft, V,
-                         temperature, u, out_len, out_tokens, workspace, static_cast<cudaStream_t>(stream));
+                         temperature, u, out_len, out_tokens, workspace, static_cast<cudaStream_t>(stream), 0, 1.f);
+}
+
+int sv_spec_accept_truncated(int B, const int32_t* row_offsets, const float* logits, int ldl, const float* row_max,
+                             const float* row_sumexp, const int32_t* row_argmax, const float* q, int ldq,
+                             const int32_t* draft, int V, float temperature, const float* u, int top_k, float top_p,
+                             int32_t* out_len, int32_t* out_tokens, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+  int st = check_accept(B, row_offsets, logits, ldl, row_max, row_sumexp, row_argmax, q, ldq, draft, V, temperature,
+                        u, out_len, out_tokens);
+  if (st) return st;
+  if (top_k < 0) return fail(SV_EINVAL, "top_k must be >= 0 (0 = no limit)");
+  if (!(top_p > 0.f && top_p <= 1.f)) return fail(SV_EINVAL, "top_p must be in (0, 1]");
+  if (!workspace) return fail(SV_EINVAL, "workspace must be non-null");
+  if (!aligned(workspace, 256)) return fail(SV_EINVAL, "workspace must be 256-byte aligned");
+  const size_t need = accept_bytes(B, row_offsets[B]);
+  if (workspace_bytes < need) return fail(SV_EINVAL, "workspace too small: %zu < %zu", workspace_bytes, need);
+  return accept_internal(B, row_offsets, logits, ldl, row_max, row_sumexp, row_argmax, q, ldq, draft, V,
+                         temperature, u, out_len, out_tokens, workspace, static_cast<cudaStream_t>(stream), top_k,
+                         top_p);
+}
+
+int sv_truncate_probs(const float* probs, int ldp, float* out, int ldo, int rows, int V, int top_k, float top_p,
+                      void* stream) {
+  if (rows < 1 || rows > 65535) return fail(SV_EINVAL, "rows must be in [1, 65535]");
+  if (V < 1 || V > (1 << 24)) return fail(SV_EINVAL, "V must be in [1, 2^24]");
+  if (!probs || !out) return fail(SV_EINVAL, "probs and out must be non-null");
+  if (ldp < V || ldo < V) return fail(SV_EINVAL, "strides must be >= V");
+  if (!aligned(probs, 4) || !aligned(out, 4)) return fail(SV_EINVAL, "misaligned rows");
+  if (top_k < 0) return fail(SV_EINVAL, "top_k must be >= 0 (0 = no limit)");
+  if (!(top_p > 0.f && top_p <= 1.f)) return fail(SV_EINVAL, "top_p must be in (0, 1]");
+  if (out != probs && ldo == ldp) {
+    const char* a = reinterpret_cast<const char*>(probs);
+    const char* b = reinterpret_cast<const char*>(out);
+    const size_t span = ((size_t)(rows - 1) * ldp + V) * 4;
+    if (a < b + span && b < a + span) return fail(SV_EINVAL, "out must equal probs or not overlap it");
+  }
+  SelectArgs a;
+  memset(&a, 0, sizeof(a));
+  a.x = probs;
+  a.ldx = ldp;
+  a.y = out;
+  a.ldy = ldo;
+  a.V = V;
+  a.mode = SEL_PROBS;
+  a.top_k = top_k;
+  a.top_p = top_p;
+  cudaError_t e = launch_select(a, rows, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "truncation launch");
+  return SV_OK;
+}
+
+int sv_logprobs(const float* logits, int ldl, int rows, int V, float temperature, const int32_t* chosen, int top_n,
+                float* chosen_logprob, int32_t* top_ids, float* top_logprobs, void* stream) {
+  if (rows < 1 || rows > 65535) return fail(SV_EINVAL, "rows must be in [1, 65535]");
+  if (V < 1 || V > (1 << 24)) return fail(SV_EINVAL, "V must be in [1, 2^24]");
+  if (!logits || ldl < V) return fail(SV_EINVAL, "logits must be non-null with ldl >= V");
+  if (!(temperature >= 0.f) || std::isinf(temperature)) return fail(SV_EINVAL, "temperature must be finite and >= 0");
+  if (top_n < 0 || top_n > 32) return fail(SV_EINVAL, "top_n must be in [0, 32]");
+  if (top_n > 0 && (!top_ids || !top_logprobs)) return fail(SV_EINVAL, "top_n > 0 needs top_ids and top_logprobs");
+  if (chosen && !chosen_logprob) return fail(SV_EINVAL, "chosen needs chosen_logprob");
+  if (!chosen && top_n == 0) return SV_OK;
+  SelectArgs a;
+  memset(&a, 0, sizeof(a));
+  a.x = logits;
+  a.ldx = ldl;
+  a.V = V;
+  a.mode = SEL_TOPN;
+  a.temperature = temperature;
+  a.chosen = chosen;
+  a.chosen_lp = chosen_logprob;
+  a.top_ids = top_ids;
+  a.top_lp = top_logprobs;
+  a.top_n = top_n;
+  cudaError_t e = launch_select(a, rows, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "logprobs launch");
+  return SV_OK;
 }
 
 int sv_spec_accept(const float* logits, int ldl, const float* row_max, const float* row_sumexp,

@@ -131,7 +131,7 @@ int check_accept(int B, const int32_t* row_offsets, const float* logits, int ldl
 int accept_internal(int B, const int32_t* offs, const float* logits, int ldl, const float* row_max,
                     const float* row_sumexp, const int32_t* row_argmax, const float* q, int ldq, const int32_t* draft,
                     int V, float temperature, const float* u, int32_t* out_len, int32_t* out_tokens, void* ws,
-                    cudaStream_t s);
+                    cudaStream_t s, int top_k = 0, float top_p = 1.f);
 cudaError_t read_and_clear_error_word(unsigned int* out);
 
 // Launchers (return cudaError_t of the launch).

@@ -7,6 +7,27 @@ namespace sv {
 
 constexpr int MAX_BATCH = 256;
 
+// Order-preserving 32-bit key of an fp32 value: larger value -> larger key;
+// -0 and +0 share a key.  Truncation bounds are expressed in these keys.
+__device__ __forceinline__ uint32_t order_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+enum : int { SEL_LOGITS = 0, SEL_PROBS = 1, SEL_TOPN = 2 };
+struct SelectArgs {
+  const float* x; int ldx;      // rows: fp32 logits (SEL_LOGITS, SEL_TOPN) or probabilities (SEL_PROBS)
+  float* y; int ldy;            // SEL_PROBS: truncated rows (may alias x)
+  int V, mode;
+  const float* row_max;         // SEL_LOGITS: row maxima (null: computed in the kernel)
+  float temperature;            // SEL_LOGITS: T > 0; SEL_TOPN: T <= 0 means 1
+  int top_k; float top_p;
+  uint32_t* out_key; int32_t* out_idx; float* out_norm;          // SEL_LOGITS: kept = key > K or (== K and index <= I)
+  const int32_t* chosen; float* chosen_lp; int32_t* top_ids; float* top_lp; int top_n;  // SEL_TOPN
+};
+cudaError_t launch_select(const SelectArgs& a, int rows, cudaStream_t s);
+
 struct AcceptParams {
   int offs[MAX_BATCH + 1];   // logits-row offsets of the requests (copied by value)
   const float* logits; int ldl;
@@ -17,6 +38,9 @@ struct AcceptParams {
   float temperature;
   const float* u;
   int32_t* out_len; int32_t* out_tokens;
+  const uint32_t* tkey;      // truncated target (or null): per logits row, kept tokens have
+  const int32_t* tidx;       //   order_key(z) > tkey, or == tkey with index <= tidx,
+  const float* tnorm;        //   and tnorm is their sum of exp((z - max) / T)
   double* chunk_sums;        // [B][nb][2]
   int* counters;             // [B], zero between calls
   int nb;                    // vocabulary chunks per request
