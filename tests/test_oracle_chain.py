@@ -150,6 +150,12 @@ def _rms(x64):
     return _bf16(x64 / np.sqrt((x64 * x64).mean(axis=1, keepdims=True) + EPS))
 
 
+def _r(x64):
+    """RMSNorm row factor 1 / sqrt(mean(x^2) + eps) (fp64): the layer folds it
+    into the consuming projection's output, one rounding per output."""
+    return 1.0 / np.sqrt((x64 * x64).mean(axis=1, keepdims=True) + EPS)
+
+
 C_Q, C_K, C_V, C_O = 2.0, 4.0, 8.0, 0.25
 B_G, B_U, B_D = 0.25, -0.5, 0.125
 
@@ -165,15 +171,14 @@ def _wired_layer(H):
 def _wired_layer_by_hand(h_bits):
     """The layer body written out for the weights of ``_wired_layer``."""
     x = _f(h_bits)
-    a = _rms(x)                                        # first RMSNorm
-    q = _bf16(C_Q * _f(a))                             # q = c_q * a
+    q = _bf16(C_Q * x * _r(x))                         # q = c_q * RMSNorm(h)
     o = _bf16(C_O * _f(q))                             # o is fed by q
     hm = _bf16(x + _f(o))                              # first residual
-    a2 = _rms(_f(hm))                                  # second RMSNorm, of the updated h
-    sigma = _f(a2).sum(axis=1, keepdims=True)
+    x2 = _f(hm)                                        # second RMSNorm, of the updated h
+    sigma = x2.sum(axis=1, keepdims=True)              # exact in fp64 for these bf16 rows
     H = x.shape[1]
-    g = _bf16(np.repeat(B_G * sigma, H, axis=1))       # gate = beta_g * sum(a2)
-    u = _bf16(np.repeat(B_U * sigma, H, axis=1))       # up = beta_u * sum(a2)
+    g = _bf16(np.repeat(B_G * sigma * _r(x2), H, axis=1))   # gate = beta_g * sum(RMSNorm(hm))
+    u = _bf16(np.repeat(B_U * sigma * _r(x2), H, axis=1))   # up = beta_u * sum(RMSNorm(hm))
     gf, uf = _f(g), _f(u)
     s = _bf16(gf / (1.0 + np.exp(-gf)) * uf)          # SwiGLU: silu(gate) * up
     d = _bf16(np.repeat(B_D * _f(s).sum(axis=1, keepdims=True), H, axis=1))
@@ -199,10 +204,11 @@ def test_layer_wiring_closed_form_catches_planted_mistakes():
     x = _f(h)
     a = _rms(x)
 
-    def tail(hm, a_mlp, swap=False, keep_residual=True):
-        sigma = _f(a_mlp).sum(axis=1, keepdims=True)
-        g = _f(_bf16(np.repeat(B_G * sigma, H, axis=1)))
-        u = _f(_bf16(np.repeat(B_U * sigma, H, axis=1)))
+    def tail(hm, mlp_in, swap=False, keep_residual=True):
+        x2 = _f(mlp_in)
+        sigma = x2.sum(axis=1, keepdims=True)
+        g = _f(_bf16(np.repeat(B_G * sigma * _r(x2), H, axis=1)))
+        u = _f(_bf16(np.repeat(B_U * sigma * _r(x2), H, axis=1)))
         if swap:
             g, u = u, g
         s = _bf16(g / (1.0 + np.exp(-g)) * u)
@@ -213,15 +219,16 @@ def test_layer_wiring_closed_form_catches_planted_mistakes():
         return _bf16(x + _f(_bf16(C_O * _f(_bf16(o_input_scale * _f(a))))))
 
     hm = hm_with(C_Q)
+    assert np.array_equal(tail(hm, hm), ref)          # the helper reproduces the closed form
     mistakes = {
-        "o fed by the normalized input": tail(hm_with(1.0), _rms(_f(hm_with(1.0)))),
-        "o fed by k": tail(hm_with(C_K), _rms(_f(hm_with(C_K)))),
-        "o fed by v": tail(hm_with(C_V), _rms(_f(hm_with(C_V)))),
-        "gate/up fed by the first RMSNorm": tail(hm, a),
-        "SwiGLU as silu(up) * gate": tail(hm, _rms(_f(hm)), swap=True),
-        "second residual dropped": tail(hm, _rms(_f(hm)), keep_residual=False),
-        "first residual dropped": tail(_bf16(_f(_bf16(C_O * C_Q * _f(a)))),
-                                       _rms(_f(_bf16(C_O * C_Q * _f(a))))),
+        "o fed by the normalized input": tail(hm_with(1.0), hm_with(1.0)),
+        "o fed by k": tail(hm_with(C_K), hm_with(C_K)),
+        "o fed by v": tail(hm_with(C_V), hm_with(C_V)),
+        "gate/up fed by the layer input": tail(hm, h),
+        "gate/up fed by the stored first RMSNorm": tail(hm, a),
+        "SwiGLU as silu(up) * gate": tail(hm, hm, swap=True),
+        "second residual dropped": tail(hm, hm, keep_residual=False),
+        "first residual dropped": tail(_bf16(_f(_bf16(C_O * C_Q * _f(a)))), _bf16(_f(_bf16(C_O * C_Q * _f(a))))),
     }
     for name, wrong in mistakes.items():
         assert not np.array_equal(wrong, ref), name
@@ -242,8 +249,8 @@ def test_round_logits_chain_and_final_norm_closed_form():
     layers = [_wired_layer(H), _wired_layer(H)]
     h1 = _wired_layer_by_hand(h0)
     h2 = _wired_layer_by_hand(h1)                     # layers applied in order, each feeding the next
-    a = _f(_rms(_f(h2)))                              # final RMSNorm before the head
-    want = (c * a[:, np.arange(V) % H]).astype(np.float32)
+    x = _f(h2)
+    want = (c * x[:, np.arange(V) % H] * _r(x)).astype(np.float32)   # final RMSNorm before the head
     hs, logits, zmax, argmax, sumexp = chain.round_logits(h0, layers, _selector_head(V, H, c), 0.7)
     assert len(hs) == 2 and np.array_equal(hs[0], h1) and np.array_equal(hs[1], h2)
     assert logits.dtype == np.float32 and np.array_equal(logits, want)
@@ -252,7 +259,7 @@ def test_round_logits_chain_and_final_norm_closed_form():
     d = (want.astype(np.float64) - want.max(axis=1, keepdims=True)) / 0.7
     assert np.allclose(sumexp, np.exp(d).sum(axis=1), rtol=1e-12)
     # without the final RMSNorm the logits would be c * h2: a different result
-    assert not np.array_equal((c * _f(h2)[:, np.arange(V) % H]).astype(np.float32), want)
+    assert not np.array_equal((c * x[:, np.arange(V) % H]).astype(np.float32), want)
 
 
 def test_verify_round_greedy_closed_form():
@@ -260,10 +267,11 @@ def test_verify_round_greedy_closed_form():
     H, V, c = 128, 128, 2.0
     h0 = synthetic.activations(r, 4, H, sigma=3.0)
     layers = [_wired_layer(H)]
-    a = _f(_rms(_f(_wired_layer_by_hand(h0))))
-    target = np.argmax((c * a).astype(np.float32), axis=1)
+    x = _f(_wired_layer_by_hand(h0))
+    a = c * x * _r(x)
+    target = np.argmax(a.astype(np.float32), axis=1)
     draft = target[:3].astype(np.int32).copy()
     draft[2] = (draft[2] + 1) % V                     # first mismatch at position 2
     out_len, tokens, logits = chain.verify_round(h0, layers, _selector_head(V, H, c), 0.0, draft)
     assert out_len == 3 and list(tokens) == [int(draft[0]), int(draft[1]), int(target[2])]
-    assert np.array_equal(logits, (c * a).astype(np.float32))
+    assert np.array_equal(logits, a.astype(np.float32))
