@@ -31,13 +31,14 @@
  *   - Nothing aborts the process and no C++ exception crosses this boundary.
  *
  * Weight format (mlx-dspark wiki page, "Key techniques": the verify kernel
- * works per weight group; group 64, affine 4-/8-bit codes, fp16 scale and
- * bias per group):
+ * works per weight group; group 64, affine 2-/4-/8-bit codes, fp16 scale and
+ * bias per group; PyPI page, "Models": 2-bit targets verify through a
+ * multi-row 2-bit matmul):
  *   wq     uint32 [N, K*bits/32]: weight (n, k) is the `bits`-wide field of word
  *          n*(K*bits/32) + k/(32/bits) at bit offset (k % (32/bits))*bits,
  *          least significant field first.
  *   scales fp16 [N, K/64], biases fp16 [N, K/64];  w[n,k] = scale*code + bias.
- *   Requirements: bits in {4, 8}, group == 64, K % 512 == 0, K <= 2^20,
+ *   Requirements: bits in {2, 4, 8}, group == 64, K % 512 == 0, K <= 2^20,
  *   1 <= N <= 2^22, wq, scales and biases 16-byte aligned (the weight rows are streamed by the tensor
  *   memory accelerator in 512-wide k chunks).
  */

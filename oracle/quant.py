@@ -2,7 +2,8 @@
 
 Weight format (mlx-dspark wiki page, "Key techniques": the verify kernel works
 per "weight group"; the group size, code widths and fp16 scale/bias come from
-the affine format of the quantized targets the pages run):
+the affine format of the quantized targets the pages run, 2-bit ones included
+(PyPI page, "Models")):
 
 * ``wq``     uint32 [N, K * bits / 32].  Weight (n, k) is the code stored in word
   ``k // (32 // bits)`` of row n, at bit offset ``(k % (32 // bits)) * bits``
@@ -22,8 +23,8 @@ GROUP = 64
 
 def unpack_codes(wq, K, bits):
     """Codes uint8 [N, K] from packed words uint32 [N, K*bits/32] (layout above)."""
-    if bits not in (4, 8):
-        raise ValueError("bits must be 4 or 8")
+    if bits not in (2, 4, 8):
+        raise ValueError("bits must be 2, 4 or 8")
     wq = np.asarray(wq, dtype=np.uint32)
     per_word = 32 // bits
     N = wq.shape[0]

@@ -15,23 +15,27 @@
 
 namespace sv {
 
+cudaError_t launch_stream_b2(const StreamParams& p, cudaStream_t s);
 cudaError_t launch_stream_b4(const StreamParams& p, cudaStream_t s);
 cudaError_t launch_stream_b8(const StreamParams& p, cudaStream_t s);
+int stream_max_grid_b2(int MP);
 int stream_max_grid_b4(int MP);
 int stream_max_grid_b8(int MP);
 
 cudaError_t launch_stream(int bits, const StreamParams& p, cudaStream_t s) {
-  return bits == 8 ? launch_stream_b8(p, s) : launch_stream_b4(p, s);
+  return bits == 8 ? launch_stream_b8(p, s) : (bits == 4 ? launch_stream_b4(p, s) : launch_stream_b2(p, s));
 }
+
+bool bits_supported(int bits) { return bits == 2 || bits == 4 || bits == 8; }
 
 int stream_max_grid(int bits, int MP) {
   static std::mutex mu;
-  static int cache[64][2][5] = {};
+  static int cache[64][3][5] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   std::lock_guard<std::mutex> lock(mu);
-  int& c = cache[dev][bits == 8][MP / 8];
-  if (!c) c = bits == 8 ? stream_max_grid_b8(MP) : stream_max_grid_b4(MP);
+  int& c = cache[dev][bits == 8 ? 2 : (bits == 4 ? 1 : 0)][MP / 8];
+  if (!c) c = bits == 8 ? stream_max_grid_b8(MP) : (bits == 4 ? stream_max_grid_b4(MP) : stream_max_grid_b2(MP));
   return c;
 }
 
@@ -167,7 +171,7 @@ int encode_weight_maps(CUtensorMap (&out)[3], const void* wq, const void* scales
 int check_weight(const uint32_t* wq, const uint16_t* scales, const uint16_t* biases, int N, int K, int bits,
                  int group, int M) {
   if (!wq || !scales || !biases) return fail(SV_EINVAL, "weight pointers must be non-null");
-  if (bits != 4 && bits != 8) return fail(SV_EUNSUPPORTED, "bits must be 4 or 8 (got %d)", bits);
+  if (!bits_supported(bits)) return fail(SV_EUNSUPPORTED, "bits must be 2, 4 or 8 (got %d)", bits);
   if (group != GROUP) return fail(SV_EUNSUPPORTED, "group size must be 64 (got %d)", group);
   if (N < 1 || N > MAX_TILES * BN) return fail(SV_EINVAL, "N out of range (got %d)", N);
   if (K < 1 || K % GROUP) return fail(SV_EINVAL, "K must be a positive multiple of 64 (got %d)", K);
@@ -183,7 +187,7 @@ int check_weight(const uint32_t* wq, const uint16_t* scales, const uint16_t* bia
 // Validation of a prepare call (everything the host can check).
 static int check_prepare(const uint16_t* x, int ldx, int M, int K, int bits, int mode, const uint16_t* x2, int ldx2,
                          void* ws) {
-  if (bits != 4 && bits != 8) return fail(SV_EUNSUPPORTED, "bits must be 4 or 8 (got %d)", bits);
+  if (!bits_supported(bits)) return fail(SV_EUNSUPPORTED, "bits must be 2, 4 or 8 (got %d)", bits);
   if (K < 1 || K % GROUP) return fail(SV_EINVAL, "K must be a positive multiple of 64 (got %d)", K);
   if (K % KC) return fail(SV_EUNSUPPORTED, "K must be a multiple of 512 (got %d)", K);
   if (K > (1 << 20)) return fail(SV_EINVAL, "K too large (got %d)", K);
@@ -303,12 +307,12 @@ using namespace sv;
 extern "C" {
 
 size_t sv_qmm_workspace_bytes(int M, int N, int K, int bits) {
-  if (M < 1 || M > MAX_M || N < 1 || N > MAX_TILES * BN || K < KC || K % KC || (bits != 4 && bits != 8)) return 0;
+  if (M < 1 || M > MAX_M || N < 1 || N > MAX_TILES * BN || K < KC || K % KC || !bits_supported(bits)) return 0;
   return qmm_bytes(M, N, K, bits, false);
 }
 
 size_t sv_lm_head_workspace_bytes(int M, int V, int K, int bits) {
-  if (M < 1 || M > MAX_M || V < 1 || V > MAX_TILES * BN || K < KC || K % KC || (bits != 4 && bits != 8)) return 0;
+  if (M < 1 || M > MAX_M || V < 1 || V > MAX_TILES * BN || K < KC || K % KC || !bits_supported(bits)) return 0;
   return qmm_bytes(M, V, K, bits, true);
 }
 

@@ -51,7 +51,7 @@ using namespace sv;
 extern "C" {
 
 size_t sv_qmm_pack_bytes(int N, int K, int bits) {
-  if (N < 1 || N > MAX_TILES * BN || K < KC || K % KC || K > (1 << 20) || (bits != 4 && bits != 8)) return 0;
+  if (N < 1 || N > MAX_TILES * BN || K < KC || K % KC || K > (1 << 20) || !bits_supported(bits)) return 0;
   return packed_bytes(N, K, bits);
 }
 
@@ -68,8 +68,10 @@ int sv_qmm_pack(const uint32_t* wq, const uint16_t* scales, const uint16_t* bias
   uint8_t* out = static_cast<uint8_t*>(packed);
   if (bits == 8)
     pack_kernel<8><<<units, 256, 0, s>>>(w, scales, biases, N, K, out);
-  else
+  else if (bits == 4)
     pack_kernel<4><<<units, 256, 0, s>>>(w, scales, biases, N, K, out);
+  else
+    pack_kernel<2><<<units, 256, 0, s>>>(w, scales, biases, N, K, out);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "pack launch");
   return SV_OK;

@@ -74,10 +74,10 @@ __global__ void __launch_bounds__(256) prep_kernel(PrepArgs a) {
   float gs = 0.f;
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
-    const int p = lane;  // element lane + 32 i of the group: block 2g + i, offset lane
+    const int pos = act_pos<BITS>(lane + 32 * i);  // element lane + 32 i of the group
     const float y = v[i] * sc;
     gs += y;
-    a.out.xp[((size_t)(2 * g + i) * MP + m) * 32 + slot_of_phys<BITS>(p)] = __float2half_rn(y);
+    a.out.xp[((size_t)(2 * g + (pos >> 5)) * MP + m) * 32 + (pos & 31)] = __float2half_rn(y);
   }
   for (int off = 16; off; off >>= 1) gs += __shfl_xor_sync(0xffffffffu, gs, off);
   if (lane == 0) {
@@ -114,6 +114,11 @@ cudaError_t launch_prep(const PrepArgs& a, int bits, int mode, cudaStream_t s) {
     if (mode == PREP_RMSNORM) return launch_prep_t<8, PREP_RMSNORM>(a, s);
     if (mode == PREP_SWIGLU) return launch_prep_t<8, PREP_SWIGLU>(a, s);
     return launch_prep_t<8, PREP_PLAIN>(a, s);
+  }
+  if (bits == 2) {
+    if (mode == PREP_RMSNORM) return launch_prep_t<2, PREP_RMSNORM>(a, s);
+    if (mode == PREP_SWIGLU) return launch_prep_t<2, PREP_SWIGLU>(a, s);
+    return launch_prep_t<2, PREP_PLAIN>(a, s);
   }
   if (mode == PREP_RMSNORM) return launch_prep_t<4, PREP_RMSNORM>(a, s);
   if (mode == PREP_SWIGLU) return launch_prep_t<4, PREP_SWIGLU>(a, s);

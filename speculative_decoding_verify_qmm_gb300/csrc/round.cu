@@ -66,7 +66,7 @@ static int check_model(const sv_model* md, int M) {
   if (!md || !md->layers) return fail(SV_EINVAL, "model and its layer array must be non-null");
   if (md->n_layers < 1) return fail(SV_EINVAL, "n_layers must be >= 1");
   if (4 * md->n_layers + 1 > MAX_PHASES) return fail(SV_EUNSUPPORTED, "at most %d layers", (MAX_PHASES - 1) / 4);
-  if (md->bits != 4 && md->bits != 8) return fail(SV_EUNSUPPORTED, "bits must be 4 or 8");
+  if (!bits_supported(md->bits)) return fail(SV_EUNSUPPORTED, "bits must be 2, 4 or 8");
   if (md->hidden < 1 || md->q_dim < 1 || md->inter < 1 || md->vocab < 2)
     return fail(SV_EINVAL, "model dimensions must be positive");
   if (!(md->rms_eps >= 0.f)) return fail(SV_EINVAL, "rms_eps must be >= 0");

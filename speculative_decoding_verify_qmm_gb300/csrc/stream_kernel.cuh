@@ -156,6 +156,27 @@ __device__ __forceinline__ void cvt4(uint32_t w, uint32_t (&P)[4]) {
   P[3] = *reinterpret_cast<uint32_t*>(&r3);
 }
 
+// Eight fp16 pairs (c - 2) from the sixteen 2-bit codes of one word; pair j =
+// (c_j, c_{8+j}).  Field j of both 16-bit halves is masked in place and OR'ed
+// into the mantissa of 1024, giving the exact fp16 value 1024 + c * 4^j' (j'
+// its position after an optional shift by 10: c * 4^j' stays below 1024 for
+// j' <= 4); one fp16 FMA by 4^-j' minus 1024 * 4^-j' + 2 leaves c - 2 exactly.
+__device__ __forceinline__ void cvt2(uint32_t w, uint32_t (&P)[8]) {
+  const uint32_t w10 = w >> 10;  // fields 5..7 of each half move to 0..2 (the high half's bits land above the masks)
+  const uint32_t src[8] = {w, w, w, w, w, w10, w10, w10};
+  const int pos[8] = {0, 1, 2, 3, 4, 0, 1, 2};
+  const unsigned short scale[5] = {0x3C00, 0x3400, 0x2C00, 0x2400, 0x1C00};  // 1, 1/4, 1/16, 1/64, 1/256
+  const unsigned short sub[5] = {0xE402, 0xDC08, 0xD420, 0xCC80, 0xC600};    // -1026, -258, -66, -18, -6
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t mask = 0x00030003u << (2 * pos[j]);
+    uint32_t x = (src[j] & mask) | 0x64006400u;
+    const __half2 r = __hfma2(*reinterpret_cast<__half2*>(&x), __half2half2(__ushort_as_half(scale[pos[j]])),
+                              __half2half2(__ushort_as_half(sub[pos[j]])));
+    P[j] = *reinterpret_cast<const uint32_t*>(&r);
+  }
+}
+
 // Slot of the element at physical offset p (0..31) of a 32-element activation
 // block, in the order the MMA fragments read the codes.
 template <int BITS>
@@ -166,6 +187,21 @@ __device__ __forceinline__ int slot_of_phys(int p) {
   }
   const int j = p & 7;  // 4-bit: slot 8t + i holds nibble (0, 4, 1, 5, 2, 6, 3, 7)[i] of block 8t
   return (p & ~7) + (j < 4 ? 2 * j : 2 * (j - 4) + 1);
+}
+// Position (block * 32 + slot) within a group's two 32-element activation
+// blocks of the group's element e (0..63).  8- and 4-bit codes keep every
+// MMA k-step inside one 32-element half of the group.  A 2-bit word holds 16
+// consecutive codes, so every step spans the whole group: thread t's word is
+// codes 16t .. 16t + 15, its pair j = (c_j, c_{8+j}) feeds step j / 2 (slots
+// 2t, 2t + 1 for even j, 2t + 8, 2t + 9 for odd j), and the steps 2b, 2b + 1
+// form block b.
+template <int BITS>
+__device__ __forceinline__ int act_pos(int e) {
+  if (BITS == 2) {
+    const int t = e >> 4, j = e & 7, hi = (e >> 3) & 1;
+    return (j >> 2) * 32 + 8 * t + ((j >> 1) & 1) * 4 + (j & 1) * 2 + hi;
+  }
+  return (e & 32) | slot_of_phys<BITS>(e & 31);
 }
 
 template <int NT>
@@ -180,7 +216,7 @@ __device__ __forceinline__ void consume_stage(const uint8_t* st, int q, int kh, 
   using C = StreamCfg<BITS, NT>;
   constexpr int MP = C::MP;
   // the tensor cores see code - OFF: 8-bit codes as 1024 + c, 4-bit ones centred as n - 8
-  constexpr float OFF = BITS == 8 ? -1024.f : 8.f;
+  constexpr float OFF = BITS == 8 ? -1024.f : (BITS == 4 ? 8.f : 2.f);
   const int gid = lane >> 2, t = lane & 3;
   const uint32_t w_base = smem_u32(st);
   const uint32_t x_base = smem_u32(st + C::X_OFF);
@@ -209,6 +245,7 @@ __device__ __forceinline__ void consume_stage(const uint8_t* st, int q, int kh, 
     b_v[h][2] = fmaf(OFF, s_v[h][2], __low2float(b23));
     b_v[h][3] = fmaf(OFF, s_v[h][3], __high2float(b23));
   }
+  uint32_t q2[4];  // 2-bit: codes of two groups, loaded at even gi
 #pragma unroll
   for (int gi = 0; gi < 4; ++gi) {
     const int gl = 4 * kh + gi;  // group index within the stage
@@ -230,6 +267,20 @@ __device__ __forceinline__ void consume_stage(const uint8_t* st, int q, int kh, 
       for (int s = 0; s < 4; ++s) {
         const uint32_t lo = qd[s >> 1][(s & 1) * 2], hi = qd[s >> 1][(s & 1) * 2 + 1];
         uint32_t a[4] = {cvt8(lo, 0x4140u), cvt8(hi, 0x4140u), cvt8(lo, 0x4342u), cvt8(hi, 0x4342u)};
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+          mma_16816(acc[j], a, bfr[s >> 1][j][(s & 1) * 2], bfr[s >> 1][j][(s & 1) * 2 + 1]);
+      }
+    } else if constexpr (BITS == 2) {
+      // the stage's one 128-byte box holds all 8 groups, a group per 16-byte
+      // chunk: one ldmatrix brings groups gl and gl + 1 for rows gid, gid + 8
+      if ((gi & 1) == 0) ldsm_x4(q2, arow + (((gl + (mi >> 1)) ^ rr) << 4));
+      uint32_t L[8], H[8];
+      cvt2(q2[2 * (gi & 1)], L);
+      cvt2(q2[2 * (gi & 1) + 1], H);
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        uint32_t a[4] = {L[2 * s], H[2 * s], L[2 * s + 1], H[2 * s + 1]};
 #pragma unroll
         for (int j = 0; j < NT; ++j)
           mma_16816(acc[j], a, bfr[s >> 1][j][(s & 1) * 2], bfr[s >> 1][j][(s & 1) * 2 + 1]);
@@ -402,8 +453,9 @@ __device__ void prepare_group(const StreamParams& p, const ActBuf& out, int grp,
     for (int c = 0; c < 2; ++c) {
       const int m = 8 * j + 2 * t + c;
       const float v0 = yv[j][c] * sc[j][c], v1 = yv[j][2 + c] * sc[j][c];
-      xp[((size_t)(2 * grp + (n_lo >> 5)) * MP + m) * 32 + slot_of_phys<BITS>(n_lo & 31)] = __float2half_rn(v0);
-      xp[((size_t)(2 * grp + (n_hi >> 5)) * MP + m) * 32 + slot_of_phys<BITS>(n_hi & 31)] = __float2half_rn(v1);
+      const int p_lo = act_pos<BITS>(n_lo), p_hi = act_pos<BITS>(n_hi);
+      xp[((size_t)(2 * grp + (p_lo >> 5)) * MP + m) * 32 + (p_lo & 31)] = __float2half_rn(v0);
+      xp[((size_t)(2 * grp + (p_hi >> 5)) * MP + m) * 32 + (p_hi & 31)] = __float2half_rn(v1);
       float s = v0 + v1;
 #pragma unroll
       for (int off = 4; off < 32; off <<= 1) s += __shfl_xor_sync(0xffffffffu, s, off);

@@ -101,6 +101,7 @@ int prepare_into(const uint16_t* x, int ldx, int M, int K, int bits, int mode, c
                  const uint16_t* w, float eps, const ActBuf& out, cudaStream_t s);
 
 int device_sm_count();
+bool bits_supported(int bits);  // code widths of the matmul kernels: 2, 4, 8
 size_t packed_bytes(int N, int K, int bits);
 // Tensor maps of one quantized weight: codes in 128-byte swizzled boxes of
 // 64 rows, scales and biases in 8-group x 64-row boxes.

@@ -23,8 +23,13 @@ import numpy as np
 
 GROUP = 64
 
-# Per-workload weight statistics: (scale_lo, scale_hi, bias_sigma)
+# Per-workload weight statistics: (scale_lo, scale_hi, bias_sigma[, centre]).
+# With a centre c the bias is -c * scale + N(0, bias_sigma): the affine form
+# of a quantiser whose group minimum sits c scales below zero, so codes are
+# centred on zero.  The 2-bit tiny workload uses it: with free N(0, 0.05)
+# biases a 2-bit row would be dominated by the biases' group sums.
 TINY_4BIT = (0.005, 0.02, 0.05)
+TINY_2BIT = (0.005, 0.02, 0.002, 1.5)
 LARGE_8BIT = (1e-4, 4e-4, 0.02)
 
 
@@ -40,10 +45,13 @@ def _bf16_bits(x):
 
 def quant_weight(r, N, K, bits, stats):
     """Host arrays {'wq', 'scales', 'biases', 'K', 'bits'} for an N x K weight."""
-    lo, hi, sigma = stats
+    lo, hi, sigma = stats[:3]
+    centre = stats[3] if len(stats) > 3 else 0.0
     wq = r.integers(0, 2 ** 32, size=(N, K * bits // 32), dtype=np.uint32)
-    scales = r.uniform(lo, hi, size=(N, K // GROUP)).astype(np.float16).view(np.uint16)
-    biases = (r.standard_normal((N, K // GROUP)) * sigma).astype(np.float16).view(np.uint16)
+    s16 = r.uniform(lo, hi, size=(N, K // GROUP)).astype(np.float16)
+    scales = s16.view(np.uint16)
+    biases = (r.standard_normal((N, K // GROUP)) * sigma - centre * s16.astype(np.float64)).astype(
+        np.float16).view(np.uint16)
     return {"wq": wq, "scales": scales, "biases": biases, "K": K, "bits": bits}
 
 
@@ -95,11 +103,13 @@ def device_quant_weight(gen, N, K, bits, stats, device="cuda"):
     and biases are drawn in fp32 and stored as fp16.
     """
     import torch
-    lo, hi, sigma = stats
+    lo, hi, sigma = stats[:3]
+    centre = stats[3] if len(stats) > 3 else 0.0
     wq = torch.randint(-2 ** 31, 2 ** 31, (N, K * bits // 32), generator=gen,
                        dtype=torch.int32, device=device)
     scales = (torch.rand((N, K // GROUP), generator=gen, device=device) * (hi - lo) + lo).to(torch.float16)
-    biases = (torch.randn((N, K // GROUP), generator=gen, device=device) * sigma).to(torch.float16)
+    biases = (torch.randn((N, K // GROUP), generator=gen, device=device) * sigma
+              - centre * scales.float()).to(torch.float16)
     return {"wq": wq, "scales": scales, "biases": biases, "K": K, "bits": bits}
 
 

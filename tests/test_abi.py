@@ -38,7 +38,7 @@ def _qmm(raw, N=64, K=512, bits=8, group=64, M=4, wq=16, x=16, y=16, ws=256, ws_
 
 def test_qmm_argument_errors_on_host(raw):
     assert _qmm(raw, bits=3) == binding.SV_EUNSUPPORTED
-    assert _qmm(raw, bits=2) == binding.SV_EUNSUPPORTED
+    assert _qmm(raw, bits=16) == binding.SV_EUNSUPPORTED
     assert _qmm(raw, group=32) == binding.SV_EUNSUPPORTED
     assert _qmm(raw, K=576) == binding.SV_EUNSUPPORTED       # multiple of 64, not of 512
     assert _qmm(raw, K=100) == binding.SV_EINVAL
@@ -123,4 +123,4 @@ def test_pack_sizes_and_argument_errors_on_host(raw):
     assert raw.sv_qmm_pack(ok["wq"], ok["s"], ok["b"], 64, 512, 8, 64, None, 1 << 20, None) == binding.SV_EINVAL
     assert raw.sv_qmm_pack(ok["wq"], ok["s"], ok["b"], 64, 512, 8, 64, P(264), 1 << 20, None) == binding.SV_EINVAL
     assert raw.sv_qmm_pack(ok["wq"], ok["s"], ok["b"], 64, 512, 8, 64, P(256), 16, None) == binding.SV_EINVAL
-    assert raw.sv_qmm_pack(ok["wq"], ok["s"], ok["b"], 64, 512, 2, 64, P(256), 1 << 20, None) == binding.SV_EUNSUPPORTED
+    assert raw.sv_qmm_pack(ok["wq"], ok["s"], ok["b"], 64, 512, 3, 64, P(256), 1 << 20, None) == binding.SV_EUNSUPPORTED

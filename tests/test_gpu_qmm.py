@@ -35,12 +35,12 @@ def test_tiny_4bit_layer(lib, M):
     assert lib.device_error() == 0
 
 
-@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("bits", [2, 4, 8])
 @pytest.mark.parametrize("N,K", [(1000, 1536), (37, 512), (130, 2048), (64, 4096)])
 @pytest.mark.parametrize("M", [1, 3, 9, 17, 24, 32])
 def test_ragged_shapes(lib, bits, N, K, M):
     r = synthetic.rng(1000 * bits + N + K + M)
-    w = synthetic.quant_weight(r, N, K, bits, synthetic.LARGE_8BIT if bits == 8 else synthetic.TINY_4BIT)
+    w = synthetic.quant_weight(r, N, K, bits, {2: synthetic.TINY_2BIT, 4: synthetic.TINY_4BIT, 8: synthetic.LARGE_8BIT}[bits])
     x = synthetic.activations(r, M, K)
     y = _run(lib, w, x)
     assert_close_bf16(host_f32_of_bf16(y), _oracle_f32(w, x), what="N=%d K=%d M=%d" % (N, K, M))

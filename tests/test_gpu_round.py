@@ -27,10 +27,13 @@ def test_fused_prepare_matches_unfused(lib, bits, M):
     y_ref = lib.qmm_verify(w["wq"], w["scales"], w["biases"], K, bits, lib.rmsnorm(h))
     torch.cuda.synchronize()
     assert_close_bf16(host_f32_of_bf16(y_fused), host_f32_of_bf16(y_ref), what="rmsnorm fused")
-    # ... and against the oracle's RMSNorm -> matmul
+    # ... against the oracle's RMSNorm -> matmul, and its folded form (one rounding of the output)
     hw = _model.host_copy(w)
     want = oq.qmm_verify(hw["wq"], hw["scales"], hw["biases"], K, bits, glue.rmsnorm(host_bf16_bits(h)))
     assert_close_bf16(host_f32_of_bf16(y_fused), quant.bf16_bits_to_f32(want), what="rmsnorm fused vs oracle")
+    hw["K"], hw["bits"] = K, bits
+    folded = quant.bf16_bits_to_f32(chain.project_normed(hw, host_bf16_bits(h)))
+    assert_close_bf16(host_f32_of_bf16(y_fused), folded, what="rmsnorm fused vs folded oracle")
     # SwiGLU fused vs standalone
     lib.qmm_prepare(h, K, bits, mode=2, x2=u, workspace=ws)
     y_fused = lib.qmm_run(w["wq"], w["scales"], w["biases"], K, bits, M, workspace=ws)
@@ -56,10 +59,12 @@ def _round(lib, model, rows_offsets, h0, T, q=None, draft=None, u=None):
 TINY = dict(hidden=1024, q_dim=1024, kv_dim=512, inter=2048, vocab=1000)
 
 
+@pytest.mark.parametrize("bits", [4, 2])
 @pytest.mark.parametrize("T", [0.0, 1.0])
-def test_tiny_model_round_matches_oracle_chain(lib, T):
+def test_tiny_model_round_matches_oracle_chain(lib, T, bits):
     n_layers, m = 3, 7
-    layers, head = _model.host_model(1300, n_layers, bits=4, stats=synthetic.TINY_4BIT, **TINY)
+    stats = synthetic.TINY_2BIT if bits == 2 else synthetic.TINY_4BIT
+    layers, head = _model.host_model(1300 + bits, n_layers, bits=bits, stats=stats, **TINY)
     dl = _model.device_layers(layers)
     dh = _model.to_device(head)
     r = synthetic.rng(1301)
@@ -67,7 +72,7 @@ def test_tiny_model_round_matches_oracle_chain(lib, T):
     hs, logits_or, _, am_or, _ = chain.round_logits(h0, layers, head, T)
     offs = [0, m + 1]
     for depth in range(1, n_layers + 1):      # per-layer hidden state via prefix models
-        model = lib.make_model(dl[:depth], dh, TINY["hidden"], TINY["q_dim"], TINY["inter"], TINY["vocab"], 4)
+        model = lib.make_model(dl[:depth], dh, TINY["hidden"], TINY["q_dim"], TINY["inter"], TINY["vocab"], bits)
         draft = synthetic.agreeing_drafts(r, am_or[:m], TINY["vocab"])
         z_q = None
         q = u = None
@@ -139,7 +144,7 @@ def _unpack_host(packed, N, K, bits):
     return codes, sc, bi
 
 
-@pytest.mark.parametrize("bits,N", [(8, 1000), (4, 1024)])
+@pytest.mark.parametrize("bits,N", [(8, 1000), (4, 1024), (2, 1000)])
 def test_pack_layout_round_trips(lib, bits, N):
     """The packed buffer holds exactly the canonical bytes in the documented order, zero rows past N."""
     r = synthetic.rng(1480 + bits)
@@ -155,10 +160,10 @@ def test_pack_layout_round_trips(lib, bits, N):
     assert not codes[N:].any() and not sc[N:].any() and not bi[N:].any()
 
 
-@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("bits", [2, 4, 8])
 def test_packed_round_is_bitwise_the_canonical_round(lib, bits):
-    layers, head = _model.host_model(1490 + bits, 2, bits=bits,
-                                     stats=synthetic.TINY_4BIT if bits == 4 else synthetic.LARGE_8BIT, **TINY)
+    layers, head = _model.host_model(1490 + bits, 2, bits=bits, stats={2: synthetic.TINY_2BIT, 4: synthetic.TINY_4BIT,
+                                                                      8: synthetic.LARGE_8BIT}[bits], **TINY)
     dl, dh = _model.device_layers(layers), _model.to_device(head)
     canon = lib.make_model(dl, dh, TINY["hidden"], TINY["q_dim"], TINY["inter"], TINY["vocab"], bits)
     pl = [{k: dict(v, packed=lib.pack(v)) for k, v in layer.items()} for layer in dl]
@@ -233,10 +238,11 @@ def test_qwen3_8b_round_per_layer_and_head(lib, model_8b, M, T):
         assert_close_bf16(host_f32_of_bf16(after), quant.bf16_bits_to_f32(want), what="layer %d" % depth)
     # vocab head on sampled rows, from the GPU's final hidden state
     lg = logits.cpu().numpy()
-    a = glue.rmsnorm(host_bf16_bits(after))
     rows = np.unique(np.concatenate([r.choice(QWEN8B["vocab"], 2048, replace=False), np.argmax(lg, axis=1)]))
     hw = _model.host_copy(head)
-    want = oq.qmm_f32(hw["wq"][rows], hw["scales"][rows], hw["biases"][rows], QWEN8B["hidden"], 8, a)
+    sub = {"wq": hw["wq"][rows], "scales": hw["scales"][rows], "biases": hw["biases"][rows], "K": QWEN8B["hidden"],
+           "bits": 8}
+    want = chain.normed_f64(sub, host_bf16_bits(after)).astype(np.float32)   # head of the final RMSNorm
     assert_close_rms(lg[:, rows], want, what="head rows")
     # accept on identical logits
     dn = draft.cpu().numpy()

@@ -19,9 +19,15 @@ def test_unpack_hand_words_4bit():
     assert quant.unpack_codes(wq, 16, 4).tolist() == [list(range(16))]
 
 
+def test_unpack_hand_words_2bit():
+    # 0xE4 = 11 10 01 00: fields 0..3 of a byte, least significant first
+    wq = np.array([[0xE4E4E4E4, 0x0000001B]], dtype=np.uint32)
+    assert quant.unpack_codes(wq, 32, 2).tolist() == [[0, 1, 2, 3] * 4 + [3, 2, 1, 0] + [0] * 12]
+
+
 def test_pack_is_inverse_of_unpack():
     r = synthetic.rng(1)
-    for bits in (4, 8):
+    for bits in (2, 4, 8):
         codes = r.integers(0, 1 << bits, size=(5, 128)).astype(np.uint8)
         assert np.array_equal(quant.unpack_codes(quant.pack_codes(codes, bits), 128, bits), codes)
 
@@ -117,9 +123,12 @@ def test_qmm_4bit_and_8bit_packings_agree():
     y4 = qmm.qmm_verify(quant.pack_codes(codes, 4), s, b, K, 4, x)
     y8 = qmm.qmm_verify(quant.pack_codes(codes, 8), s, b, K, 8, x)
     assert np.array_equal(y4, y8)
+    c2 = codes & 3                                 # codes that fit 2 bits: all three packings agree
+    y2 = qmm.qmm_verify(quant.pack_codes(c2, 2), s, b, K, 2, x)
+    assert np.array_equal(y2, qmm.qmm_verify(quant.pack_codes(c2, 8), s, b, K, 8, x))
 
 
-@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("bits", [2, 4, 8])
 def test_qmm_brute_force_tiny(bits):
     r = synthetic.rng(7 + bits)
     N, K, M = 3, 128, 2
