@@ -134,6 +134,28 @@ int sv_qmm_run(const uint32_t* wq, const uint16_t* scales, const uint16_t* biase
                int M, uint16_t* y, int ldy, const uint16_t* residual, int ldr, void* workspace,
                size_t workspace_bytes, void* stream);
 
+/* Gather form for mixture-of-experts targets (PyPI page, "Results at a
+ * glance": on an MoE target every verify row pulls in its own set of
+ * experts; wiki page, "Key techniques": each weight group is dequantized once
+ * and reused across rows).  P (row, expert) pairs:
+ *   Y[p, :] = X[pair_rows[p], :] * W_{pair_experts[p]}^T,   p = 0 .. P-1,
+ * with the arithmetic of sv_qmm_verify.  The experts are stacked along N:
+ * wq [E*N, K*bits/32], scales / biases [E*N, K/64] (expert e owns rows
+ * e*N .. e*N + N - 1), in the weight format above.  x bf16 [M, K] (stride
+ * ldx), M <= 32; pair_rows and pair_experts are DEVICE int32 [P] (1 <= P <=
+ * 1024); y bf16 [P, N] (stride ldy).  The pairs are grouped by expert on the
+ * device: every selected expert is streamed once and applied to all rows
+ * routed to it.  An expert may receive at most M pairs; a pair with a row
+ * outside [0, M) or an expert outside [0, E), or an expert's pairs beyond M,
+ * leave their output rows untouched and set the bad-input bit that
+ * sv_device_error() reports.  1 <= E <= 4096.
+ * Workspace: sv_gather_qmm_workspace_bytes(P, M, N, K, E, bits), 256-byte
+ * aligned; no zero-fill needed. */
+size_t sv_gather_qmm_workspace_bytes(int P, int M, int N, int K, int E, int bits);
+int sv_gather_qmm(const uint32_t* wq, const uint16_t* scales, const uint16_t* biases, int E, int N, int K, int bits,
+                  int group, const uint16_t* x, int ldx, int M, const int32_t* pair_rows, const int32_t* pair_experts,
+                  int P, uint16_t* y, int ldy, void* workspace, size_t workspace_bytes, void* stream);
+
 /* -------------------------------------------------------------- lm_head ---
  * The vocab head of the round with its row softmax statistics fused in
  * (wiki page, "Architecture": the draft is compared against the target's own

@@ -70,3 +70,18 @@ def target_probs(logits_row, temperature):
     z = np.asarray(logits_row, dtype=np.float64)
     e = np.exp((z - z.max()) / float(temperature))
     return e / e.sum()
+
+
+def gather_qmm(experts, x_bf16, pair_rows, pair_experts):
+    """bf16 [P, N]: row p = X[pair_rows[p]] times expert pair_experts[p]'s weight.
+
+    mlx-dspark PyPI page, "Results at a glance" (MoE rows): each verify row
+    selects its own experts.  ``experts`` is a list of E weight dicts
+    ``{"wq", "scales", "biases", "K", "bits"}`` of the same shape; every pair is
+    the plain verify matmul of one activation row with one expert."""
+    x = np.asarray(x_bf16, dtype=np.uint16)
+    out = []
+    for r, e in zip(pair_rows, pair_experts):
+        w = experts[int(e)]
+        out.append(qmm_verify(w["wq"], w["scales"], w["biases"], w["K"], w["bits"], x[int(r):int(r) + 1])[0])
+    return np.stack(out)

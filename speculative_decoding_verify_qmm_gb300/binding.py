@@ -109,6 +109,10 @@ _SIGNATURES = {
                                    _c_void_p]),
     "sv_logprobs": (_c_int, [_c_void_p, _c_int, _c_int, _c_int, _c_float, _c_void_p, _c_int, _c_void_p, _c_void_p,
                              _c_void_p, _c_void_p]),
+    "sv_gather_qmm_workspace_bytes": (_c_size_t, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
+    "sv_gather_qmm": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_void_p,
+                               _c_int, _c_int, _c_void_p, _c_void_p, _c_int, _c_void_p, _c_int, _c_void_p,
+                               _c_size_t, _c_void_p]),
     "sv_expected_committed": (ctypes.c_double, [ctypes.c_double, _c_int]),
     "sv_best_cap": (_c_int, [ctypes.c_double, _c_int, _c_f64_p, _c_f64_p, ctypes.c_double, _c_int_p, _c_f64_p]),
     "sv_verify_knee": (_c_int, [_c_f64_p, _c_int, ctypes.c_double, _c_int_p]),
@@ -447,6 +451,26 @@ class Library:
                                         int(top_n), _ptr(clp), _ptr(ids) if top_n else None,
                                         _ptr(tlp) if top_n else None, _stream(stream)))
         return clp, ids, tlp
+
+    # --------------------------------------------------------------- gather
+    def gather_qmm(self, wq, scales, biases, E, K, bits, x, pair_rows, pair_experts, y=None, workspace=None,
+                   stream=None):
+        """Stacked expert weights [E*N, ...]; pair_rows / pair_experts int32 device tensors [P]."""
+        import torch
+        N = wq.shape[0] // E
+        M, P = x.shape[0], pair_rows.shape[0]
+        if y is None:
+            y = torch.empty((P, N), dtype=torch.bfloat16, device=x.device)
+        if workspace is None:
+            nbytes = self.lib.sv_gather_qmm_workspace_bytes(P, M, N, K, E, bits)
+            if nbytes == 0:
+                raise SVError(SV_EINVAL, "sv_gather_qmm_workspace_bytes: unsupported sizes")
+            workspace = self.workspace(nbytes, x.device)
+        self.check(self.lib.sv_gather_qmm(_ptr(wq), _ptr(scales), _ptr(biases), E, N, K, bits, 64, _ptr(x),
+                                          x.stride(0), M, _ptr(pair_rows), _ptr(pair_experts), P, _ptr(y), y.stride(0),
+                                          _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                          _stream(stream)))
+        return y
 
     # --------------------------------------------------------------- philox
     def philox_uniforms(self, seed, subsequence, offset, n, out=None, stream=None):

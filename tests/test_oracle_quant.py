@@ -160,3 +160,25 @@ def test_qmm_rows_are_independent_and_linear():
     # Y(-X) = -Y(X): negating a bf16 flips its sign bit exactly
     yn = qmm.qmm_f32(w["wq"], w["scales"], w["biases"], K, 8, x ^ np.uint16(0x8000))
     assert np.array_equal(yn, -y)
+
+
+def test_gather_qmm_pairs_are_independent_verify_matmuls():
+    r = synthetic.rng(12)
+    E, N, K, M = 5, 24, 128, 4
+    experts = [synthetic.quant_weight(r, N, K, 4, synthetic.TINY_4BIT) for _ in range(E)]
+    x = synthetic.activations(r, M, K)
+    rows = np.array([0, 0, 1, 3, 2, 3, 0])
+    exps = np.array([4, 1, 1, 0, 4, 4, 2])
+    y = qmm.gather_qmm(experts, x, rows, exps)
+    assert y.shape == (len(rows), N)
+    # one expert and the identity routing is the plain verify matmul
+    w = experts[1]
+    assert np.array_equal(qmm.gather_qmm(experts, x, np.arange(M), np.full(M, 1)),
+                          qmm.qmm_verify(w["wq"], w["scales"], w["biases"], K, 4, x))
+    # a pair's result depends only on its own (row, expert): permuting the pairs permutes the rows
+    perm = r.permutation(len(rows))
+    assert np.array_equal(qmm.gather_qmm(experts, x, rows[perm], exps[perm]), y[perm])
+    # brute force on one pair from the dequantized expert
+    wh = quant.dequantize(experts[4]["wq"], experts[4]["scales"], experts[4]["biases"], K, 4).astype(np.float64)
+    want = quant.f32_to_bf16_bits((quant.bf16_bits_to_f32(x[2]).astype(np.float64) @ wh.T).astype(np.float32))
+    assert np.array_equal(y[4], want)
