@@ -124,8 +124,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-static int encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t dim0, uint64_t dim1,
-                     uint64_t stride1, uint32_t box0, uint32_t box1, CUtensorMapSwizzle sw) {
+int encode_tiled_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t dim0, uint64_t dim1,
+                    uint64_t stride1, uint32_t box0, uint32_t box1, CUtensorMapSwizzle sw) {
   auto fn = encode_fn();
   if (!fn) return fail(SV_ECUDA, "cuTensorMapEncodeTiled is not available from the driver");
   const cuuint64_t dims[2] = {dim0, dim1};
@@ -160,10 +160,10 @@ int encode_weight_maps(CUtensorMap (&out)[3], const void* wq, const void* scales
   const uint64_t row_bytes = (uint64_t)K * bits / 8, G = (uint64_t)(K / GROUP);
   int st = encode_codes(&out[0], wq, row_bytes, (uint64_t)N, (uint32_t)(KC * bits / 8 / 128));
   if (st) return st;
-  st = encode_2d(&out[1], CU_TENSOR_MAP_DATA_TYPE_UINT16, scales, G, (uint64_t)N, G * 2, GPS, BN,
+  st = encode_tiled_2d(&out[1], CU_TENSOR_MAP_DATA_TYPE_UINT16, scales, G, (uint64_t)N, G * 2, GPS, BN,
                  CU_TENSOR_MAP_SWIZZLE_NONE);
   if (st) return st;
-  return encode_2d(&out[2], CU_TENSOR_MAP_DATA_TYPE_UINT16, biases, G, (uint64_t)N, G * 2, GPS, BN,
+  return encode_tiled_2d(&out[2], CU_TENSOR_MAP_DATA_TYPE_UINT16, biases, G, (uint64_t)N, G * 2, GPS, BN,
                    CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
@@ -307,7 +307,8 @@ using namespace sv;
 extern "C" {
 
 size_t sv_qmm_workspace_bytes(int M, int N, int K, int bits) {
-  if (M < 1 || M > MAX_M || N < 1 || N > MAX_TILES * BN || K < KC || K % KC || !bits_supported(bits)) return 0;
+  if (M < 1 || M > WIDE_MAX_M || N < 1 || N > MAX_TILES * BN || K < KC || K % KC || !bits_supported(bits)) return 0;
+  if (M > MAX_M) return wide_bytes(M, N, K, bits);
   return qmm_bytes(M, N, K, bits, false);
 }
 
@@ -352,9 +353,28 @@ int sv_qmm_run(const uint32_t* wq, const uint16_t* scales, const uint16_t* biase
                           static_cast<cudaStream_t>(stream));
 }
 
+static int qmm_verify_wide(const uint32_t* wq, const uint16_t* scales, const uint16_t* biases, int N, int K, int bits,
+                           int group, const uint16_t* x, int ldx, int M, uint16_t* y, int ldy,
+                           const uint16_t* residual, int ldr, void* workspace, size_t workspace_bytes, void* stream) {
+  int st = check_weight(wq, scales, biases, N, K, bits, group, 1);
+  if (st) return st;
+  if (!x || !y || !workspace) return fail(SV_EINVAL, "x, y and workspace must be non-null");
+  if (ldx < K || ldy < N || (residual && ldr < N)) return fail(SV_EINVAL, "ldx must be >= K, ldy and ldr >= N");
+  if (!aligned(x, 2) || !aligned(y, 2) || (residual && !aligned(residual, 2)))
+    return fail(SV_EINVAL, "misaligned x, y or residual");
+  if (!aligned(workspace, 256)) return fail(SV_EINVAL, "workspace must be 256-byte aligned");
+  const size_t need = wide_bytes(M, N, K, bits);
+  if (workspace_bytes < need) return fail(SV_EINVAL, "workspace too small: %zu < %zu", workspace_bytes, need);
+  return wide_qmm(wq, scales, biases, N, K, bits, x, ldx, M, y, ldy, residual, ldr, workspace,
+                  static_cast<cudaStream_t>(stream));
+}
+
 int sv_qmm_verify(const uint32_t* wq, const uint16_t* scales, const uint16_t* biases, int N, int K, int bits,
                   int group, const uint16_t* x, int ldx, int M, uint16_t* y, int ldy, const uint16_t* residual,
                   int ldr, void* workspace, size_t workspace_bytes, void* stream) {
+  if (M > MAX_M && M <= WIDE_MAX_M)
+    return qmm_verify_wide(wq, scales, biases, N, K, bits, group, x, ldx, M, y, ldy, residual, ldr, workspace,
+                           workspace_bytes, stream);
   int st = check_weight(wq, scales, biases, N, K, bits, group, M);
   if (st) return st;
   st = check_prepare(x, ldx, M, K, bits, PREP_PLAIN, nullptr, 0, workspace);

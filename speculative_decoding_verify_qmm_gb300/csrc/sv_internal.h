@@ -21,7 +21,8 @@ constexpr int NCW = 8;           // consumer warps per CTA: 4 row quarters x 2 k
 constexpr int NEW = 4;           // epilogue warps per CTA: one per row quarter
 constexpr int XPW = NCW + 1 + NEW;  // the activation-copy warp
 constexpr int QMM_THREADS = (NCW + 1 + NEW + 1) * 32;  // consumers, weight producer, epilogue warps, activation producer
-constexpr int MAX_M = 32;        // rows per verify block handled by the kernels
+constexpr int MAX_M = 32;        // rows per verify block handled by the weight-streaming kernels
+constexpr int WIDE_MAX_M = 512;  // rows per block of the tensor-memory kernel (sv_qmm_verify, M > 32)
 constexpr int MAX_PHASES = 272;  // matmuls per launch (64 layers x 4 projections + head, with room)
 
 enum PrepMode : int { PREP_PLAIN = 0, PREP_RMSNORM = 1, PREP_SWIGLU = 2 };
@@ -108,6 +109,13 @@ size_t packed_bytes(int N, int K, int bits);
 int encode_weight_maps(CUtensorMap (&out)[3], const void* wq, const void* scales, const void* biases, int N, int K,
                        int bits);
 int fail(int status, const char* fmt, ...);
+int encode_tiled_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t dim0, uint64_t dim1,
+                    uint64_t stride1_bytes, uint32_t box0, uint32_t box1, CUtensorMapSwizzle sw);
+// The wide-block matmul (33 <= M <= 512, tcgen05): workspace size and launch.
+size_t wide_bytes(int M, int N, int K, int bits);
+int wide_qmm(const uint32_t* wq, const uint16_t* scales, const uint16_t* biases, int N, int K, int bits,
+             const uint16_t* x, int ldx, int M, uint16_t* y, int ldy, const uint16_t* residual, int ldr, void* ws,
+             cudaStream_t s);
 int check_weight(const uint32_t* wq, const uint16_t* scales, const uint16_t* biases, int N, int K, int bits,
                  int group, int M);
 int cuda_fail(cudaError_t e, const char* what);

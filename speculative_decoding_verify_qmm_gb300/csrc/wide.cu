@@ -1,0 +1,396 @@
+// Wide-block quantized matmul on the 5th-generation tensor cores (33..512 rows).
+//
+// mlx-dspark PyPI page, "Prompt processing (prefill)": wide blocks (prompt
+// chunks, long verify blocks) dequantize the weights once per block rather
+// than once per output tile; wiki page, "Key techniques": one weight group is
+// dequantized once and reused across every row.  Past 32 rows the contraction
+// is dense enough for tcgen05.mma: a CTA owns 128 weight rows, four warps
+// dequantize each 64-wide k-step of them into fp16 in shared memory (the
+// 128-byte-swizzled K-major layout the tensor cores read), one thread issues
+// tcgen05.mma with the weights as the 128-row A operand and the block's rows
+// as the N operand (up to 256 per instruction), accumulating in fp32 in tensor
+// memory, and the same four warps read the accumulators back (tcgen05.ld) for
+// the epilogue.  A producer warp keeps a ring of stages filled by TMA: the
+// stage's raw codes, scales and biases, and the matching 64-wide slice of the
+// activations, prepared once as fp16 scaled by a power of two per row (exact
+// for every bf16 value; the scale is undone in the epilogue).
+//
+// Arithmetic: w = fp16(fp32(fp32(scale * code) + bias)) - the oracle's fp32
+// weight, rounded once more to fp16 (relative error <= 2^-11) - times the exact
+// fp16 activations, fp32 accumulation.  When a projection has too few 128-row
+// tiles to fill the GPU, k is split across CTAs and a second kernel adds the
+// fp32 partials in split order.
+#include <cstring>
+
+#include "sv_internal.h"
+#include "sv_ptx.cuh"
+#include "sv_tc05.cuh"
+
+namespace sv {
+
+constexpr int WT = 128;            // weight rows per tile (the MMA's M)
+constexpr int WK = 64;             // k per stage: one 128-byte fp16 row
+constexpr int W_THREADS = 192;     // warps 0-3 dequant + epilogue, 4 TMA producer, 5 MMA issue + TMEM
+constexpr int W_MAX_STAGES = 6;
+
+struct WideParams {
+  CUtensorMap tm_codes, tm_scales, tm_biases, tm_x;
+  int N, K, M, Mpad, stages, splits, ks_total;
+  int nchunk, chunk;                 // the block's rows as nchunk MMA operands of `chunk` rows (<= 256)
+  int stage_bytes, codes_bytes;      // codes_bytes: one stage's raw codes (128 rows)
+  uint32_t tmem_cols;
+  const float* inv_scale;            // [Mpad]: 2^-e of each activation row
+  __nv_bfloat16* y; int ldy;         // splits == 1: the output
+  const __nv_bfloat16* res; int ldr; // optional residual (splits == 1)
+  float* partials;                   // splits > 1: [splits][M][N] fp32
+};
+
+// Stage layout (1024-aligned): [A fp16 128 x 64, swizzled][X fp16 Mpad x 64, swizzled][codes][scales][biases]
+__host__ __device__ inline int wide_x_off() { return WT * 128; }
+__host__ __device__ inline int wide_codes_off(int Mpad) { return WT * 128 + Mpad * 128; }
+
+template <int BITS>
+__device__ __forceinline__ uint32_t code_at(const uint8_t* row, int k) {
+  if (BITS == 8) return row[k];
+  if (BITS == 4) return (row[k >> 1] >> ((k & 1) * 4)) & 15u;
+  return (row[k >> 2] >> ((k & 3) * 2)) & 3u;
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(W_THREADS, 1) wide_kernel(const __grid_constant__ WideParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t full_bar[W_MAX_STAGES], deq_bar[W_MAX_STAGES], empty_bar[W_MAX_STAGES], acc_bar, fin_bar;
+  __shared__ uint32_t s_tmem;
+  __shared__ int abort_flag;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  volatile int* abort_v = &abort_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int S = p.stages;
+  const int tile = blockIdx.x / p.splits, split = blockIdx.x % p.splits;
+  const int n0 = tile * WT;
+  const int ks0 = (int)((long long)split * p.ks_total / p.splits);
+  const int ks1 = (int)((long long)(split + 1) * p.ks_total / p.splits);
+  const int nk = ks1 - ks0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&deq_bar[s], 128);
+      mbar_init(&empty_bar[s], 1);
+    }
+    mbar_init(&acc_bar, 1);
+    mbar_init(&fin_bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(&s_tmem, p.tmem_cols);
+    tmem_relinquish();
+  }
+  tc05_fence_before();
+  __syncthreads();
+  tc05_fence_after();
+  const uint32_t tmem = s_tmem;
+  pdl_wait();  // the prepared activations come from the previous launch
+
+  if (warp == 4) {
+    // ============================================================ producer
+    if (lane == 0) {
+      const uint64_t pol_w = l2_evict_first(), pol_x = l2_evict_last();
+      const uint32_t tx = (uint32_t)(p.codes_bytes + 2 * WT * 8 * 2 + p.Mpad * 128);
+      bool bad = false;
+      int i = 0;
+      for (; i < nk; ++i) {
+        const int s = i % S, ks = ks0 + i;
+        if (i >= S && !mbar_wait_bounded(&empty_bar[s], ((i / S) - 1) & 1, abort_v)) {
+          if (!*abort_v) raise_error(ERR_TIMEOUT_EMPTY);
+          *abort_v = 1;
+          bad = true;
+          break;
+        }
+        uint8_t* st = smem + s * p.stage_bytes;
+        uint8_t* codes = st + wide_codes_off(p.Mpad);
+        mbar_arrive_expect_tx(&full_bar[s], tx);
+        tma_load_2d(codes, &p.tm_codes, &full_bar[s], ks * WK * BITS / 8, n0, pol_w);
+        tma_load_2d(codes + p.codes_bytes, &p.tm_scales, &full_bar[s], (ks / 8) * 8, n0, pol_w);
+        tma_load_2d(codes + p.codes_bytes + WT * 16, &p.tm_biases, &full_bar[s], (ks / 8) * 8, n0, pol_w);
+        for (int c = 0; c < p.nchunk; ++c)
+          tma_load_2d(st + wide_x_off() + c * p.chunk * 128, &p.tm_x, &full_bar[s], ks * WK, c * p.chunk, pol_x);
+      }
+      // copies in flight land before the CTA may finish (bounded)
+      if (!bad && !*abort_v) {
+        for (int k = (i - S > 0 ? i - S : 0); k < i; ++k) mbar_wait_bounded(&full_bar[k % S], (k / S) & 1, abort_v);
+      } else {
+        const unsigned long long t0 = global_ns();
+        while (global_ns() - t0 < 50000ull) __nanosleep(1000);
+      }
+    }
+  } else if (warp == 5) {
+    // ============================================================ MMA issue
+    if (lane == 0) {
+      int issued = 0;
+      for (int i = 0; i < nk && !*abort_v; ++i) {
+        const int s = i % S;
+        if (!mbar_wait_bounded(&full_bar[s], (i / S) & 1, abort_v) ||
+            !mbar_wait_bounded(&deq_bar[s], (i / S) & 1, abort_v)) {
+          if (!*abort_v) raise_error(ERR_TIMEOUT_FULL);
+          *abort_v = 1;
+          break;
+        }
+        tc05_fence_after();
+        const uint32_t a_base = smem_u32(smem + s * p.stage_bytes);
+        const uint32_t x_base = a_base + wide_x_off();
+#pragma unroll
+        for (int kk = 0; kk < WK / 16; ++kk) {
+          const uint64_t a_desc = sw128_desc(a_base + kk * 32);
+          for (int c = 0; c < p.nchunk; ++c) {
+            const uint64_t b_desc = sw128_desc(x_base + c * p.chunk * 128 + kk * 32);
+            tc05_mma_f16(tmem + c * p.chunk, a_desc, b_desc, f16_idesc(WT, p.chunk), i > 0 || kk > 0);
+          }
+        }
+        tc05_commit(&empty_bar[s]);  // the stage is free once these MMAs have read it
+        ++issued;
+      }
+      tc05_commit(&acc_bar);   // the accumulators are final once every MMA has completed
+      // no MMA may still be running when the tensor memory is freed: this wait
+      // ignores the abort flag and ends only on completion or the time limit
+      tc05_commit(&fin_bar);
+      volatile int never = 0;
+      mbar_wait_bounded(&fin_bar, 0, &never);
+      (void)issued;
+    }
+  } else {
+    // ================================================= dequant, then epilogue
+    const int r = threadIdx.x;  // weight row within the tile (warps 0-3)
+    for (int i = 0; i < nk; ++i) {
+      const int s = i % S, ks = ks0 + i;
+      if (*abort_v) break;
+      if (!mbar_wait_bounded(&full_bar[s], (i / S) & 1, abort_v)) {
+        if (!*abort_v) raise_error(ERR_TIMEOUT_FULL);
+        *abort_v = 1;
+        break;
+      }
+      uint8_t* st = smem + s * p.stage_bytes;
+      const uint8_t* codes = st + wide_codes_off(p.Mpad) + r * (WK * BITS / 8);
+      const __half* sc = reinterpret_cast<const __half*>(st + wide_codes_off(p.Mpad) + p.codes_bytes);
+      const __half* bi = sc + WT * 8;
+      const float scale = __half2float(sc[r * 8 + (ks & 7)]);
+      const float bias = __half2float(bi[r * 8 + (ks & 7)]);
+      uint8_t local[WK * BITS / 8];
+#pragma unroll
+      for (int j = 0; j < WK * BITS / 8; j += 16)
+        *reinterpret_cast<uint4*>(local + j) = *reinterpret_cast<const uint4*>(codes + j);
+      uint8_t* arow = st + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint32_t packed[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const float w0 = __fadd_rn(__fmul_rn(scale, (float)code_at<BITS>(local, 8 * c + 2 * h)), bias);
+          const float w1 = __fadd_rn(__fmul_rn(scale, (float)code_at<BITS>(local, 8 * c + 2 * h + 1)), bias);
+          const __half2 hw = __floats2half2_rn(w0, w1);
+          packed[h] = *reinterpret_cast<const uint32_t*>(&hw);
+        }
+        *reinterpret_cast<uint4*>(arow + ((c ^ (r & 7)) << 4)) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+      }
+      fence_proxy_async_smem();  // the tensor cores read these writes through the async proxy
+      mbar_arrive(&deq_bar[s]);
+    }
+    // epilogue: this warp's 32 TMEM lanes are weight rows n0 + 32 warp .. + 31
+    bool ok = !*abort_v && mbar_wait_bounded(&acc_bar, 0, abort_v);
+    ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld is warp-collective: the whole warp reads or none
+    tc05_fence_after();
+    const int n = n0 + 32 * warp + lane;
+    if (ok) {
+      for (int col = 0; col < p.Mpad; col += 16) {
+        float v[16];
+        tmem_ld16(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)col, v);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int m = col + j;
+          if (m < p.M && n < p.N) {
+            const float val = v[j] * p.inv_scale[m];
+            if (p.splits > 1) {
+              p.partials[((size_t)split * p.M + m) * p.N + n] = val;
+            } else {
+              float out = __bfloat162float(__float2bfloat16_rn(val));
+              if (p.res) out = __bfloat162float(p.res[(size_t)m * p.ldr + n]) + out;
+              p.y[(size_t)m * p.ldy + n] = __float2bfloat16_rn(out);
+            }
+          }
+        }
+      }
+    } else if (!*abort_v) {
+      raise_error(ERR_TIMEOUT_FULL);
+    }
+  }
+  tc05_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc05_fence_after();
+    tmem_dealloc(tmem, p.tmem_cols);
+  }
+}
+
+// Activations for the wide kernel: fp16 x * 2^e per row (e = 15 - exponent of
+// the row's max |x|), 2^-e per row; rows M .. Mpad-1 zero.  One block per row.
+__global__ void __launch_bounds__(256) wide_prep_kernel(const __nv_bfloat16* __restrict__ x, int ldx, int M, int K,
+                                                        __half* __restrict__ x16, float* __restrict__ inv) {
+  pdl_trigger();
+  pdl_wait();
+  const int m = blockIdx.x, tid = threadIdx.x;
+  __shared__ float s_max[8];
+  float mx = 0.f;
+  if (m < M)
+    for (int k = tid; k < K; k += 256) mx = fmaxf(mx, fabsf(__bfloat162float(x[(size_t)m * ldx + k])));
+  for (int off = 16; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  if ((tid & 31) == 0) s_max[tid >> 5] = mx;
+  __syncthreads();
+  mx = 0.f;
+  for (int w = 0; w < 8; ++w) mx = fmaxf(mx, s_max[w]);
+  int e = 0;
+  if (mx > 0.f && mx <= 3.0e38f) {
+    int E;
+    frexpf(mx, &E);
+    e = 15 - E;
+    e = e > 100 ? 100 : (e < -100 ? -100 : e);
+  }
+  const float sc = ldexpf(1.f, e);
+  for (int k = tid; k < K; k += 256)
+    x16[(size_t)m * K + k] = __float2half_rn(m < M ? __bfloat162float(x[(size_t)m * ldx + k]) * sc : 0.f);
+  if (tid == 0) inv[m] = ldexpf(1.f, -e);
+}
+
+// Sum of the split partials in split order, then bf16 (with the optional residual).
+__global__ void __launch_bounds__(256) wide_finish_kernel(const float* __restrict__ part, int splits, int M, int N,
+                                                          const __nv_bfloat16* __restrict__ res, int ldr,
+                                                          __nv_bfloat16* __restrict__ y, int ldy) {
+  pdl_trigger();
+  pdl_wait();
+  const size_t total = (size_t)M * N;
+  for (size_t i = (size_t)blockIdx.x * 256 + threadIdx.x; i < total; i += (size_t)gridDim.x * 256) {
+    float acc = 0.f;
+    for (int j = 0; j < splits; ++j) acc += part[(size_t)j * total + i];
+    const int m = (int)(i / N), n = (int)(i % N);
+    float out = __bfloat162float(__float2bfloat16_rn(acc));
+    if (res) out = __bfloat162float(res[(size_t)m * ldr + n]) + out;
+    y[(size_t)m * ldy + n] = __float2bfloat16_rn(out);
+  }
+}
+
+struct WidePlan {
+  int Mpad, nchunk, chunk, stages, splits, tiles, ks_total, stage_bytes, smem;
+  size_t x16, inv, partials, total;
+};
+
+static WidePlan wide_plan(int M, int N, int K, int bits, int sms) {
+  WidePlan w;
+  // an MMA takes at most 256 rows (a multiple of 16): wider blocks are two equal chunks
+  w.nchunk = M > 256 ? 2 : 1;
+  w.Mpad = w.nchunk == 1 ? 16 * ((M + 15) / 16) : 32 * ((M + 31) / 32);
+  w.chunk = w.Mpad / w.nchunk;
+  const int codes = WT * WK * bits / 8;
+  w.stage_bytes = (wide_codes_off(w.Mpad) + codes + 2 * WT * 16 + 1023) / 1024 * 1024;
+  const int budget = 226 * 1024 - 1024;  // 1 KB of it aligns the stages
+  w.stages = budget / w.stage_bytes;
+  if (w.stages > W_MAX_STAGES) w.stages = W_MAX_STAGES;
+  w.smem = 1024 + w.stages * w.stage_bytes;
+  w.tiles = (N + WT - 1) / WT;
+  w.ks_total = K / WK;
+  int splits = 1;
+  if (sms > 0 && w.tiles < sms) {
+    splits = sms / w.tiles;
+    const int max_split = w.ks_total / 8 > 0 ? w.ks_total / 8 : 1;  // at least 8 k-steps per split
+    if (splits > max_split) splits = max_split;
+    if (splits < 1) splits = 1;
+  }
+  w.splits = splits;
+  size_t off = COUNTER_BYTES;
+  w.x16 = off;      off = align256(off + (size_t)w.Mpad * K * 2);
+  w.inv = off;      off = align256(off + (size_t)w.Mpad * 4);
+  w.partials = off; off = align256(off + (splits > 1 ? (size_t)splits * M * N * 4 : 0));
+  w.total = off;
+  return w;
+}
+
+template <int BITS>
+static cudaError_t launch_wide_t(const WideParams& p, int grid, int smem, cudaStream_t s) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    // every plan needs at most 226 KB of dynamic shared memory (the rest of
+    // the 227 KB opt-in limit holds the kernel's barriers)
+    cudaError_t e = cudaFuncSetAttribute(wide_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         226 * 1024);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pdl_config(dim3(grid), dim3(W_THREADS), smem, s, attr);
+  return cudaLaunchKernelEx(&cfg, wide_kernel<BITS>, p);
+}
+
+size_t wide_bytes(int M, int N, int K, int bits) { return wide_plan(M, N, K, bits, device_sm_count()).total; }
+
+int wide_qmm(const uint32_t* wq, const uint16_t* scales, const uint16_t* biases, int N, int K, int bits,
+             const uint16_t* x, int ldx, int M, uint16_t* y, int ldy, const uint16_t* residual, int ldr, void* ws,
+             cudaStream_t s) {
+  const int sms = device_sm_count();
+  if (sms <= 0) return fail(SV_ECUDA, "no CUDA device");
+  const WidePlan w = wide_plan(M, N, K, bits, sms);
+  if (w.stages < 2) return fail(SV_EUNSUPPORTED, "rows %d need more shared memory than a CTA has", M);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  __half* x16 = reinterpret_cast<__half*>(base + w.x16);
+  float* inv = reinterpret_cast<float*>(base + w.inv);
+  {
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = pdl_config(dim3(w.Mpad), dim3(256), 0, s, attr);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, wide_prep_kernel, reinterpret_cast<const __nv_bfloat16*>(x), ldx, M, K,
+                                       x16, inv);
+    if (e != cudaSuccess) return cuda_fail(e, "wide preparation launch");
+  }
+  static thread_local WideParams p;
+  memset(static_cast<void*>(&p), 0, sizeof(p));
+  const uint64_t row_bytes = (uint64_t)K * bits / 8, G = (uint64_t)(K / GROUP);
+  int st = encode_tiled_2d(&p.tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, row_bytes, (uint64_t)N, row_bytes,
+                         (uint32_t)(WK * bits / 8), WT, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (!st) st = encode_tiled_2d(&p.tm_scales, CU_TENSOR_MAP_DATA_TYPE_UINT16, scales, G, (uint64_t)N, G * 2, 8, WT,
+                              CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (!st) st = encode_tiled_2d(&p.tm_biases, CU_TENSOR_MAP_DATA_TYPE_UINT16, biases, G, (uint64_t)N, G * 2, 8, WT,
+                              CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (!st) st = encode_tiled_2d(&p.tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x16, (uint64_t)K, (uint64_t)w.Mpad,
+                              (uint64_t)K * 2, WK, w.chunk, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (st) return st;
+  p.N = N;
+  p.K = K;
+  p.M = M;
+  p.Mpad = w.Mpad;
+  p.nchunk = w.nchunk;
+  p.chunk = w.chunk;
+  p.stages = w.stages;
+  p.splits = w.splits;
+  p.ks_total = w.ks_total;
+  p.stage_bytes = w.stage_bytes;
+  p.codes_bytes = WT * WK * bits / 8;
+  uint32_t cols = 32;
+  while ((int)cols < w.Mpad) cols <<= 1;
+  p.tmem_cols = cols;
+  p.inv_scale = inv;
+  p.y = reinterpret_cast<__nv_bfloat16*>(y);
+  p.ldy = ldy;
+  p.res = reinterpret_cast<const __nv_bfloat16*>(residual);
+  p.ldr = ldr;
+  p.partials = w.splits > 1 ? reinterpret_cast<float*>(base + w.partials) : nullptr;
+  const int grid = w.tiles * w.splits;
+  cudaError_t e = bits == 8 ? launch_wide_t<8>(p, grid, w.smem, s)
+                            : (bits == 4 ? launch_wide_t<4>(p, grid, w.smem, s) : launch_wide_t<2>(p, grid, w.smem, s));
+  if (e != cudaSuccess) return cuda_fail(e, "wide matmul launch");
+  if (w.splits > 1) {
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = pdl_config(dim3(4 * sms), dim3(256), 0, s, attr);
+    e = cudaLaunchKernelEx(&cfg, wide_finish_kernel, (const float*)p.partials, w.splits, M, N, p.res, ldr, p.y, ldy);
+    if (e != cudaSuccess) return cuda_fail(e, "wide finish launch");
+  }
+  return SV_OK;
+}
+
+}  // namespace sv

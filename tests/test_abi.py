@@ -42,7 +42,7 @@ def test_qmm_argument_errors_on_host(raw):
     assert _qmm(raw, group=32) == binding.SV_EUNSUPPORTED
     assert _qmm(raw, K=576) == binding.SV_EUNSUPPORTED       # multiple of 64, not of 512
     assert _qmm(raw, K=100) == binding.SV_EINVAL
-    assert _qmm(raw, M=33) == binding.SV_EUNSUPPORTED
+    assert _qmm(raw, M=513) == binding.SV_EUNSUPPORTED
     assert _qmm(raw, M=0) == binding.SV_EINVAL
     assert _qmm(raw, N=0) == binding.SV_EINVAL
     assert _qmm(raw, wq=0) == binding.SV_EINVAL

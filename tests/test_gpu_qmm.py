@@ -109,9 +109,9 @@ def test_host_rejections(lib):
     r = synthetic.rng(10)
     w = synthetic.quant_weight(r, 128, 1024, 8, synthetic.LARGE_8BIT)
     dw = dev_weight(w)
-    x = dev_bf16(synthetic.activations(r, 33, 1024))
+    x = dev_bf16(synthetic.activations(r, 513, 1024))
     with pytest.raises(SVError) as e:
-        lib.qmm_verify(dw["wq"], dw["scales"], dw["biases"], 1024, 8, x)
+        lib.qmm_verify(dw["wq"], dw["scales"], dw["biases"], 1024, 8, x, workspace=lib.workspace(1 << 20))
     assert e.value.status == 2
     small = lib.workspace(256)
     with pytest.raises(SVError) as e:
