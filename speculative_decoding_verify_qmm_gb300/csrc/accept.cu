@@ -61,13 +61,16 @@ __global__ void __launch_bounds__(ACC_THREADS) accept_kernel(const AcceptParams 
   const int V = p.V;
 
   if (!(p.temperature > 0.f)) {
-    if (chunk != 0 || tid != 0) return;
-    int a = m;
-    for (int i = 0; i < m; ++i)
-      if (p.draft[qd0 + i] != p.row_argmax[r0 + i]) { a = i; break; }
-    for (int i = 0; i < a; ++i) p.out_tokens[r0 + i] = p.draft[qd0 + i];
-    p.out_tokens[r0 + a] = p.row_argmax[r0 + a];
-    p.out_len[b] = a + 1;
+    // greedy: one lane per draft (m <= 31); the first mismatch is the lowest set bit of a ballot
+    if (chunk != 0 || tid >= 32) return;
+    const int d = tid < m ? p.draft[qd0 + tid] : 0;
+    const unsigned miss = __ballot_sync(0xffffffffu, tid < m && d != p.row_argmax[r0 + tid]);
+    const int a = miss ? __ffs(miss) - 1 : m;
+    if (tid < a) p.out_tokens[r0 + tid] = d;
+    if (tid == 0) {
+      p.out_tokens[r0 + a] = p.row_argmax[r0 + a];
+      p.out_len[b] = a + 1;
+    }
     return;
   }
 

@@ -137,3 +137,72 @@ def test_out_of_range_draft_is_flagged(lib):
     _gpu(lib, z, q, draft, 1.0, u)
     assert lib.device_error() != 0
     assert lib.device_error() == 0          # reading clears it
+
+
+def test_greedy_m31_full_vocab_every_mismatch_position(lib):
+    """The warp-wide first-mismatch reduction at its widest (m = 31 drafts)."""
+    r = synthetic.rng(820)
+    m, V = 31, 151936
+    z = (r.standard_normal((m + 1, V)) * 2).astype(np.float32)
+    target = np.argmax(z, axis=1)
+    for pos in [0, 1, 15, 29, 30, None]:
+        draft = target[:m].astype(np.int32).copy()
+        if pos is not None:
+            draft[pos] = (draft[pos] + 1) % V
+            draft[pos + 1:] = r.integers(0, V, m - pos - 1)   # anything after the first mismatch
+        assert _gpu(lib, z, None, draft, 0.0, None) == tuple(oa.greedy_accept(z, draft))
+    assert lib.device_error() == 0
+
+
+def test_draft_equal_to_target_always_accepts(lib):
+    """q = p (the target's own distribution, in fp32): p/q = 1 up to rounding, so
+    every draft is accepted except where |u - p/q| < 1e-6."""
+    r = synthetic.rng(821)
+    m, V, T = 15, 151936, 1.0
+    z = (r.standard_normal((m + 1, V)) * 2).astype(np.float32)
+    q = np.stack([oq_target(z[i], T) for i in range(m)]).astype(np.float32)
+    for _ in range(3):
+        draft = np.asarray([int(r.choice(V, p=q[i].astype(np.float64) / q[i].astype(np.float64).sum()))
+                            for i in range(m)], np.int32)
+        u = synthetic.accept_uniforms(r, m + 1)
+        det = oa.sampled_accept_detail(z, q, draft, T, u)
+        got = _gpu(lib, z, q, draft, T, u)
+        if got != (det["out_len"], det["tokens"]):
+            assert _exempt(det, u)
+        else:
+            assert got[0] == m + 1                         # all accepted, then the bonus draw
+    assert lib.device_error() == 0
+
+
+def oq_target(z_row, T):
+    from oracle import qmm as oq
+    return oq.target_probs(z_row, T)
+
+
+def test_small_residual_draw_is_valid(lib):
+    """q = p (1 +- 1e-4), renormalised: a rejection leaves a residual max(0, p - q)
+    whose total Z is ~1e-4.  Decisions are bit-exact (ratios are far from u);
+    the drawn token carries positive residual weight and sits where u * Z falls
+    in the oracle's cumulative weights, to within the kernel's fp32 rounding of
+    p (about 1e-7 of p per token, a few 1e-4 of a Z this small)."""
+    r = synthetic.rng(822)
+    V, T = 32768, 1.0
+    for trial in range(6):
+        z = (r.standard_normal((2, V)) * 2).astype(np.float32)
+        p0 = oq_target(z[0], T)
+        q0 = p0 * (1.0 + 1e-4 * np.sign(r.standard_normal(V)))
+        q0 = np.ascontiguousarray((q0 / q0.sum()).astype(np.float32).reshape(1, V))
+        d = int(np.argmax(np.where(q0[0] > p0, p0, 0.0)))   # a likely token with q > p: p/q < 1
+        draft = np.asarray([d], np.int32)
+        u = np.asarray([0.99995, r.random()], np.float32)   # rejected: u > p/q ~ 1 - 1e-4
+        det = oa.sampled_accept_detail(z, q0, draft, T, u)
+        assert det["reject"] == 0 and det["weights_kind"] == "residual" and det["Z"] < 1e-3
+        n, toks = _gpu(lib, z, q0, draft, T, u)
+        assert n == 1
+        k = toks[0]
+        res = np.maximum(0.0, p0 - q0[0].astype(np.float64))
+        assert res[k] > 0
+        c = np.cumsum(res) / res.sum()
+        lo, hi = (c[k - 1] if k else 0.0), c[k]
+        assert lo - 2e-3 <= float(u[1]) <= hi + 2e-3, (trial, lo, float(u[1]), hi)
+    assert lib.device_error() == 0
