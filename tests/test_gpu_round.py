@@ -254,3 +254,94 @@ def test_qwen3_8b_round_per_layer_and_head(lib, model_8b, M, T):
         want_acc = tuple(oa.greedy_accept(lg, dn))
     assert (int(n[0]), toks[:n[0]].tolist()) == want_acc
     assert lib.device_error() == 0
+
+
+def _check_round_layers(lib, layers, head, shape, offs, h0, T, depths, q=None, draft=None, u=None, bits=8):
+    """Run the round at each prefix depth and compare the checked layers (given the
+    GPU's own input of that layer) and the head's sampled rows with the oracle."""
+    r = synthetic.rng(sum(depths))
+
+    def run(depth):
+        model = lib.make_model(layers[:depth], head, shape["hidden"], shape["q_dim"], shape["inter"], shape["vocab"],
+                               bits)
+        return _round(lib, model, offs, h0, T, q=q, draft=draft, u=u)
+
+    for depth in depths:
+        before = host_bf16_bits(run(depth - 1)[0]) if depth > 1 else host_bf16_bits(h0)
+        after, logits, n, toks = run(depth)
+        lay = _model.split_device_layer(layers[depth - 1], shape["q_dim"], shape["kv_dim"], shape["inter"])
+        want = chain.layer_forward(before, lay)
+        assert_close_bf16(host_f32_of_bf16(after), quant.bf16_bits_to_f32(want), what="layer %d" % depth)
+    lg = logits.cpu().numpy()
+    rows = np.unique(np.concatenate([r.choice(shape["vocab"], 2048, replace=False), np.argmax(lg, axis=1)]))
+    hw = _model.host_copy(head)
+    sub = {"wq": hw["wq"][rows], "scales": hw["scales"][rows], "biases": hw["biases"][rows], "K": shape["hidden"],
+           "bits": bits}
+    assert_close_rms(lg[:, rows], chain.normed_f64(sub, host_bf16_bits(after)).astype(np.float32), what="head rows")
+    return lg, n, toks
+
+
+QWEN4B = dict(hidden=2560, q_dim=4096, kv_dim=1024, inter=9728, vocab=151936)
+
+
+@pytest.mark.parametrize("M,T", [(8, 0.0), (32, 0.7)])
+def test_qwen3_4b_shaped_4bit_round(lib, M, T):
+    """4B-shaped 4-bit target (hidden 2560, q 4096, kv 1024, inter 9728, the full
+    151936-row head): a 3-layer prefix model, every layer and the head checked."""
+    layers, head = _model.device_random_model(2100 + M, 3, bits=4, stats=synthetic.LARGE_8BIT, **QWEN4B)
+    r = synthetic.rng(2101 + M)
+    m = M - 1
+    h0 = dev_bf16(synthetic.activations(r, M, QWEN4B["hidden"]))
+    q = u = None
+    if T > 0:
+        _, qn = synthetic.logits_and_draft_probs(r, m, QWEN4B["vocab"])
+        q = torch.from_numpy(qn).cuda()
+        u = torch.from_numpy(synthetic.accept_uniforms(r, M)).cuda()
+    draft = torch.from_numpy(r.integers(0, QWEN4B["vocab"], m).astype(np.int32)).cuda()
+    lg, n, toks = _check_round_layers(lib, layers, head, QWEN4B, [0, M], h0, T, (1, 2, 3), q=q, draft=draft, u=u,
+                                      bits=4)
+    dn = draft.cpu().numpy()
+    if T > 0:
+        det = oa.sampled_accept_detail(lg, q.cpu().numpy(), dn, T, u.cpu().numpy())
+        want = (det["out_len"], det["tokens"])
+    else:
+        want = tuple(oa.greedy_accept(lg, dn))
+    assert (int(n[0]), toks[:n[0]].tolist()) == want
+    assert lib.device_error() == 0
+
+
+QWEN27B = dict(hidden=5120, q_dim=6144, kv_dim=1024, inter=17408, vocab=151936)
+
+
+def test_27b_class_64_layer_batched_round(lib):
+    """27B-class 8-bit shapes in one 64-layer launch (257 phases), B = 4 requests x
+    (1 + 7) rows = 32 rows, T = 1.0, each request's uniforms from its own Philox
+    stream; layers 1, 32 and 64 and the head against the oracle, then each
+    request's accept on the GPU's logits."""
+    layers, head = _model.device_random_model(2700, 64, bits=8, stats=synthetic.LARGE_8BIT, **QWEN27B)
+    r = synthetic.rng(2701)
+    B, rows = 4, 8
+    M, m = B * rows, rows - 1
+    offs = [b * rows for b in range(B + 1)]
+    h0 = dev_bf16(synthetic.activations(r, M, QWEN27B["hidden"]))
+    _, qn = synthetic.logits_and_draft_probs(r, B * m, QWEN27B["vocab"])
+    q = torch.from_numpy(qn).cuda()
+    u = torch.cat([lib.philox_uniforms(2702, b, 0, rows) for b in range(B)])
+    draft = torch.from_numpy(r.integers(0, QWEN27B["vocab"], B * m).astype(np.int32)).cuda()
+    lg, n, toks = _check_round_layers(lib, layers, head, QWEN27B, offs, h0, 1.0, (1, 32, 64), q=q, draft=draft, u=u)
+    uh, dn, qh = u.cpu().numpy(), draft.cpu().numpy(), q.cpu().numpy()
+    for b in range(B):
+        det = oa.sampled_accept_detail(lg[offs[b]:offs[b + 1]], qh[b * m:(b + 1) * m], dn[b * m:(b + 1) * m], 1.0,
+                                       uh[offs[b]:offs[b + 1]])
+        got = (int(n[b]), toks[offs[b]:offs[b] + n[b]].tolist())
+        assert got == (det["out_len"], det["tokens"]) or _near_tie(det, uh[offs[b]:offs[b + 1]]), b
+    del layers, head
+    torch.cuda.empty_cache()
+    assert lib.device_error() == 0
+
+
+def _near_tie(det, u):
+    for i, rr in enumerate(det["ratios"]):
+        if np.isfinite(rr) and abs(float(u[i]) - rr) < 1e-6:
+            return True
+    return bool(np.min(np.abs(det["cdf"] - det["theta"])) < 1e-6 * det["Z"])
