@@ -388,6 +388,74 @@ __device__ __forceinline__ bool partial_take(float* buf, float (&v)[NT][4], int 
   return true;
 }
 
+// Adds the partials of contributors c_first .. c_last (those with a non-empty
+// unit range) in CTA order, fetching up to B of them at once: their loads are
+// issued together and the wait is one L2 round trip, not one per contributor.
+// Each contributor's words are read, added and zeroed as a whole, in CTA
+// order, so the sum is bitwise reproducible.
+template <int NT>
+__device__ __forceinline__ bool partial_take_many(float* partials, int q, int c_first, int c_last, int total,
+                                                  int grid, float (&v)[NT][4], int lane, volatile int* abort_v,
+                                                  volatile int* abort_g) {
+  constexpr int B = 2;                 // contributors fetched together (registers: B x NT x 4 per lane)
+  constexpr int RF = 16 * 8 * NT;      // one quarter's floats
+  unsigned* const w0 = reinterpret_cast<unsigned*>(partials) + (size_t)q * RF + lane;
+  for (int c0 = c_first; c0 <= c_last; c0 += B) {
+    bool need[B], have[B];
+    unsigned got[B][NT][4];
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
+      const int c = c0 + b;
+      need[b] = c <= c_last && unit_start(c + 1, total, grid) > unit_start(c, total, grid);
+      have[b] = !need[b];
+    }
+    // contributor c's words for this quarter and lane: w0 + c * (2 * 4 * RF) + (j * 4 + e) * 32
+    auto word = [&](int b, int j, int e) { return w0 + (size_t)(c0 + b) * (8 * RF) + (j * 4 + e) * 32; };
+    const unsigned long long t0 = global_ns();
+    for (unsigned it = 0;; ++it) {
+      bool all = true;
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        if (have[b]) continue;
+        bool ok = true;
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            got[b][j][e] = __ldcv(word(b, j, e));
+            ok &= got[b][j][e] != 0u;
+          }
+        have[b] = ok;
+        all &= ok;
+      }
+      if (all) break;
+      if ((it & 15u) == 15u) {
+        if (*abort_v) return false;
+        const unsigned long long dt = global_ns() - t0;
+        if (dt > 20000ull && *abort_g) return false;
+        if (dt > WAIT_LIMIT_NS) {
+          raise_error(ERR_TIMEOUT_FULL);
+          *abort_v = 1;
+          *abort_g = 1;
+          return false;
+        }
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
+      if (!need[b]) continue;
+#pragma unroll
+      for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          v[j][e] += __uint_as_float(~got[b][j][e]);
+          __stcg(word(b, j, e), 0u);
+        }
+    }
+  }
+  return true;
+}
+
 constexpr int EPI_BAR = 5;       // the four epilogue warps
 constexpr int EPI_THREADS = 128;
 
@@ -976,11 +1044,15 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
         if (finisher) {
           // ---- fetch ahead: contributors' partials (they met this tile first)
           if (c_last != fin) {
-            for (int c = fin + 1; c <= c_last; ++c)
-              if (unit_start(c + 1, total, pg) > unit_start(c, total, pg) &&
-                  !partial_take<NT>(p.partials + (((size_t)c * 2) * 4 + q) * C::RED_FLOATS, part, lane, abort_v,
-                                    abort_g))
-                break;
+            if constexpr (NT <= 3) {  // contributors fetched two at a time
+              partial_take_many<NT>(p.partials, q, fin + 1, c_last, total, pg, part, lane, abort_v, abort_g);
+            } else {                  // 32 rows: one at a time (the batched form's registers would spill)
+              for (int c = fin + 1; c <= c_last; ++c)
+                if (unit_start(c + 1, total, pg) > unit_start(c, total, pg) &&
+                    !partial_take<NT>(p.partials + (((size_t)c * 2) * 4 + q) * C::RED_FLOATS, part, lane, abort_v,
+                                      abort_g))
+                  break;
+            }
           }
           // ... the hidden-state rows of a residual tile, the partner of a gate tile
           if (ph.kind == PH_RESID) {

@@ -4,13 +4,13 @@
 // chunks, long verify blocks) dequantize the weights once per block rather
 // than once per output tile; wiki page, "Key techniques": one weight group is
 // dequantized once and reused across every row.  Past 32 rows the contraction
-// is dense enough for tcgen05.mma: a CTA owns 128 weight rows, four warps
+// is dense enough for tcgen05.mma: a CTA owns 128 weight rows, eight warps
 // dequantize each 64-wide k-step of them into fp16 in shared memory (the
 // 128-byte-swizzled K-major layout the tensor cores read), one thread issues
 // tcgen05.mma with the weights as the 128-row A operand and the block's rows
 // as the N operand (up to 256 per instruction), accumulating in fp32 in tensor
-// memory, and the same four warps read the accumulators back (tcgen05.ld) for
-// the epilogue.  A producer warp keeps a ring of stages filled by TMA: the
+// memory, and the dequantizing warps read the accumulators back (tcgen05.ld)
+// for the epilogue.  A producer warp keeps a ring of stages filled by TMA: the
 // stage's raw codes, scales and biases, and the matching 64-wide slice of the
 // activations, prepared once as fp16 scaled by a power of two per row (exact
 // for every bf16 value; the scale is undone in the epilogue).
@@ -30,7 +30,10 @@ namespace sv {
 
 constexpr int WT = 128;            // weight rows per tile (the MMA's M)
 constexpr int WK = 64;             // k per stage: one 128-byte fp16 row
-constexpr int W_THREADS = 192;     // warps 0-3 dequant + epilogue, 4 TMA producer, 5 MMA issue + TMEM
+constexpr int W_DQ = 8;            // dequantizing (then epilogue) warps: two threads per weight row
+constexpr int W_PROD = W_DQ;       // the TMA producer warp
+constexpr int W_MMA = W_DQ + 1;    // the MMA-issuing warp, which also owns the tensor memory
+constexpr int W_THREADS = (W_DQ + 2) * 32;
 constexpr int W_MAX_STAGES = 6;
 
 struct WideParams {
@@ -75,7 +78,7 @@ __global__ void __launch_bounds__(W_THREADS, 1) wide_kernel(const __grid_constan
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full_bar[s], 1);
-      mbar_init(&deq_bar[s], 128);
+      mbar_init(&deq_bar[s], W_DQ * 32);
       mbar_init(&empty_bar[s], 1);
     }
     mbar_init(&acc_bar, 1);
@@ -83,7 +86,7 @@ __global__ void __launch_bounds__(W_THREADS, 1) wide_kernel(const __grid_constan
     abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == W_MMA) {
     tmem_alloc(&s_tmem, p.tmem_cols);
     tmem_relinquish();
   }
@@ -93,7 +96,7 @@ __global__ void __launch_bounds__(W_THREADS, 1) wide_kernel(const __grid_constan
   const uint32_t tmem = s_tmem;
   pdl_wait();  // the prepared activations come from the previous launch
 
-  if (warp == 4) {
+  if (warp == W_PROD) {
     // ============================================================ producer
     if (lane == 0) {
       const uint64_t pol_w = l2_evict_first(), pol_x = l2_evict_last();
@@ -125,7 +128,7 @@ __global__ void __launch_bounds__(W_THREADS, 1) wide_kernel(const __grid_constan
         while (global_ns() - t0 < 50000ull) __nanosleep(1000);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == W_MMA) {
     // ============================================================ MMA issue
     if (lane == 0) {
       int issued = 0;
@@ -161,7 +164,9 @@ __global__ void __launch_bounds__(W_THREADS, 1) wide_kernel(const __grid_constan
     }
   } else {
     // ================================================= dequant, then epilogue
-    const int r = threadIdx.x;  // weight row within the tile (warps 0-3)
+    // thread t: weight row r = t % 128 of the tile, k half h = t / 128 (32 codes)
+    const int r = threadIdx.x & (WT - 1), h = threadIdx.x / WT;
+    constexpr int HB = WK * BITS / 16;  // code bytes of half a row's k-step
     for (int i = 0; i < nk; ++i) {
       const int s = i % S, ks = ks0 + i;
       if (*abort_v) break;
@@ -171,40 +176,49 @@ __global__ void __launch_bounds__(W_THREADS, 1) wide_kernel(const __grid_constan
         break;
       }
       uint8_t* st = smem + s * p.stage_bytes;
-      const uint8_t* codes = st + wide_codes_off(p.Mpad) + r * (WK * BITS / 8);
+      const uint8_t* codes = st + wide_codes_off(p.Mpad) + r * (WK * BITS / 8) + h * HB;
       const __half* sc = reinterpret_cast<const __half*>(st + wide_codes_off(p.Mpad) + p.codes_bytes);
       const __half* bi = sc + WT * 8;
       const float scale = __half2float(sc[r * 8 + (ks & 7)]);
       const float bias = __half2float(bi[r * 8 + (ks & 7)]);
-      uint8_t local[WK * BITS / 8];
+      uint8_t local[HB < 16 ? 16 : HB];
+      if constexpr (HB >= 16) {
 #pragma unroll
-      for (int j = 0; j < WK * BITS / 8; j += 16)
-        *reinterpret_cast<uint4*>(local + j) = *reinterpret_cast<const uint4*>(codes + j);
+        for (int j = 0; j < HB; j += 16)
+          *reinterpret_cast<uint4*>(local + j) = *reinterpret_cast<const uint4*>(codes + j);
+      } else {  // 2-bit: 8 bytes per half row
+        *reinterpret_cast<uint2*>(local) = *reinterpret_cast<const uint2*>(codes);
+      }
       uint8_t* arow = st + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
+      for (int cc = 0; cc < 4; ++cc) {
+        const int c = 4 * h + cc;  // 16-byte chunk (8 fp16) of the row's 128 bytes
         uint32_t packed[4];
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          const float w0 = __fadd_rn(__fmul_rn(scale, (float)code_at<BITS>(local, 8 * c + 2 * h)), bias);
-          const float w1 = __fadd_rn(__fmul_rn(scale, (float)code_at<BITS>(local, 8 * c + 2 * h + 1)), bias);
+        for (int e = 0; e < 4; ++e) {
+          const float w0 = __fadd_rn(__fmul_rn(scale, (float)code_at<BITS>(local, 8 * cc + 2 * e)), bias);
+          const float w1 = __fadd_rn(__fmul_rn(scale, (float)code_at<BITS>(local, 8 * cc + 2 * e + 1)), bias);
           const __half2 hw = __floats2half2_rn(w0, w1);
-          packed[h] = *reinterpret_cast<const uint32_t*>(&hw);
+          packed[e] = *reinterpret_cast<const uint32_t*>(&hw);
         }
         *reinterpret_cast<uint4*>(arow + ((c ^ (r & 7)) << 4)) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
       }
       fence_proxy_async_smem();  // the tensor cores read these writes through the async proxy
       mbar_arrive(&deq_bar[s]);
     }
-    // epilogue: this warp's 32 TMEM lanes are weight rows n0 + 32 warp .. + 31
+    // epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31 (weight rows), the
+    // first half of the columns (block rows) for w < 4, the second for w >= 4
     bool ok = !*abort_v && mbar_wait_bounded(&acc_bar, 0, abort_v);
     ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld is warp-collective: the whole warp reads or none
     tc05_fence_after();
-    const int n = n0 + 32 * warp + lane;
+    const int lq = warp & 3;
+    const int n = n0 + 32 * lq + lane;
+    const int split_col = (p.Mpad / 32) * 16;  // a multiple of 16: the loads read 16 columns at a time
+    const int col0 = (warp >> 2) ? split_col : 0, col1 = (warp >> 2) ? p.Mpad : split_col;
     if (ok) {
-      for (int col = 0; col < p.Mpad; col += 16) {
+      for (int col = col0; col < col1; col += 16) {
         float v[16];
-        tmem_ld16(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)col, v);
+        tmem_ld16(tmem + ((uint32_t)(32 * lq) << 16) + (uint32_t)col, v);
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int m = col + j;
@@ -226,7 +240,7 @@ __global__ void __launch_bounds__(W_THREADS, 1) wide_kernel(const __grid_constan
   }
   tc05_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == W_MMA) {
     tc05_fence_after();
     tmem_dealloc(tmem, p.tmem_cols);
   }
@@ -297,12 +311,24 @@ static WidePlan wide_plan(int M, int N, int K, int bits, int sms) {
   w.smem = 1024 + w.stages * w.stage_bytes;
   w.tiles = (N + WT - 1) / WT;
   w.ks_total = K / WK;
+  // k splits, in units of the whole GPU's compute time for the projection:
+  // waves of CTAs (sms / tiles * ceil(tiles * s / sms) / s) plus, for s > 1,
+  // the HBM time of writing and re-reading the fp32 partials, which relative
+  // to the compute time is about 0.27 * s * 4096 / K (8 B per output per
+  // split against 2 K flops per output at this part's bf16 rate and copy
+  // bandwidth); at least 8 k-steps per split
   int splits = 1;
-  if (sms > 0 && w.tiles < sms) {
-    splits = sms / w.tiles;
-    const int max_split = w.ks_total / 8 > 0 ? w.ks_total / 8 : 1;  // at least 8 k-steps per split
-    if (splits > max_split) splits = max_split;
-    if (splits < 1) splits = 1;
+  if (sms > 0) {
+    const int max_split = w.ks_total / 8 > 0 ? w.ks_total / 8 : 1;
+    double best = 1e30;
+    for (int sp = 1; sp <= max_split && sp <= 16; ++sp) {
+      const double waves = (double)sms / w.tiles * (double)((w.tiles * sp + sms - 1) / sms) / sp;
+      const double cost = waves + (sp > 1 ? 0.27 * sp * 4096.0 / K : 0.0);
+      if (cost < best - 1e-12) {
+        best = cost;
+        splits = sp;
+      }
+    }
   }
   w.splits = splits;
   size_t off = COUNTER_BYTES;
