@@ -39,7 +39,7 @@ constexpr int W_MAX_STAGES = 6;
 struct WideParams {
   CUtensorMap tm_codes, tm_scales, tm_biases, tm_x;
   int N, K, M, Mpad, stages, splits, ks_total;
-  int nchunk, chunk;                 // the block's rows as nchunk MMA operands of `chunk` rows (<= 256)
+  int mchunks, chunk;                // the block's rows in mchunks CTAs of `chunk` rows (<= 256, one MMA operand)
   int stage_bytes, codes_bytes;      // codes_bytes: one stage's raw codes (128 rows)
   uint32_t tmem_cols;
   const float* inv_scale;            // [Mpad]: 2^-e of each activation row
@@ -48,9 +48,9 @@ struct WideParams {
   float* partials;                   // splits > 1: [splits][M][N] fp32
 };
 
-// Stage layout (1024-aligned): [A fp16 128 x 64, swizzled][X fp16 Mpad x 64, swizzled][codes][scales][biases]
+// Stage layout (1024-aligned): [A fp16 128 x 64, swizzled][X fp16 rows x 64, swizzled][codes][scales][biases]
 __host__ __device__ inline int wide_x_off() { return WT * 128; }
-__host__ __device__ inline int wide_codes_off(int Mpad) { return WT * 128 + Mpad * 128; }
+__host__ __device__ inline int wide_codes_off(int rows) { return WT * 128 + rows * 128; }
 
 template <int BITS>
 __device__ __forceinline__ uint32_t code_at(const uint8_t* row, int k) {
@@ -69,8 +69,10 @@ __global__ void __launch_bounds__(W_THREADS, 1) wide_kernel(const __grid_constan
   volatile int* abort_v = &abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = p.stages;
-  const int tile = blockIdx.x / p.splits, split = blockIdx.x % p.splits;
-  const int n0 = tile * WT;
+  // CTAs of one weight tile are adjacent (its row chunks and k splits run together and share it in L2)
+  const int per_tile = p.mchunks * p.splits;
+  const int tile = blockIdx.x / per_tile, mc = (blockIdx.x % per_tile) / p.splits, split = blockIdx.x % p.splits;
+  const int n0 = tile * WT, m0 = mc * p.chunk;
   const int ks0 = (int)((long long)split * p.ks_total / p.splits);
   const int ks1 = (int)((long long)(split + 1) * p.ks_total / p.splits);
   const int nk = ks1 - ks0;
@@ -100,7 +102,7 @@ __global__ void __launch_bounds__(W_THREADS, 1) wide_kernel(const __grid_constan
     // ============================================================ producer
     if (lane == 0) {
       const uint64_t pol_w = l2_evict_first(), pol_x = l2_evict_last();
-      const uint32_t tx = (uint32_t)(p.codes_bytes + 2 * WT * 8 * 2 + p.Mpad * 128);
+      const uint32_t tx = (uint32_t)(p.codes_bytes + 2 * WT * 8 * 2 + p.chunk * 128);
       bool bad = false;
       int i = 0;
       for (; i < nk; ++i) {
@@ -112,13 +114,12 @@ __global__ void __launch_bounds__(W_THREADS, 1) wide_kernel(const __grid_constan
           break;
         }
         uint8_t* st = smem + s * p.stage_bytes;
-        uint8_t* codes = st + wide_codes_off(p.Mpad);
+        uint8_t* codes = st + wide_codes_off(p.chunk);
         mbar_arrive_expect_tx(&full_bar[s], tx);
         tma_load_2d(codes, &p.tm_codes, &full_bar[s], ks * WK * BITS / 8, n0, pol_w);
         tma_load_2d(codes + p.codes_bytes, &p.tm_scales, &full_bar[s], (ks / 8) * 8, n0, pol_w);
         tma_load_2d(codes + p.codes_bytes + WT * 16, &p.tm_biases, &full_bar[s], (ks / 8) * 8, n0, pol_w);
-        for (int c = 0; c < p.nchunk; ++c)
-          tma_load_2d(st + wide_x_off() + c * p.chunk * 128, &p.tm_x, &full_bar[s], ks * WK, c * p.chunk, pol_x);
+        tma_load_2d(st + wide_x_off(), &p.tm_x, &full_bar[s], ks * WK, m0, pol_x);
       }
       // copies in flight land before the CTA may finish (bounded)
       if (!bad && !*abort_v) {
@@ -146,10 +147,7 @@ __global__ void __launch_bounds__(W_THREADS, 1) wide_kernel(const __grid_constan
 #pragma unroll
         for (int kk = 0; kk < WK / 16; ++kk) {
           const uint64_t a_desc = sw128_desc(a_base + kk * 32);
-          for (int c = 0; c < p.nchunk; ++c) {
-            const uint64_t b_desc = sw128_desc(x_base + c * p.chunk * 128 + kk * 32);
-            tc05_mma_f16(tmem + c * p.chunk, a_desc, b_desc, f16_idesc(WT, p.chunk), i > 0 || kk > 0);
-          }
+          tc05_mma_f16(tmem, a_desc, sw128_desc(x_base + kk * 32), f16_idesc(WT, p.chunk), i > 0 || kk > 0);
         }
         tc05_commit(&empty_bar[s]);  // the stage is free once these MMAs have read it
         ++issued;
@@ -176,8 +174,8 @@ __global__ void __launch_bounds__(W_THREADS, 1) wide_kernel(const __grid_constan
         break;
       }
       uint8_t* st = smem + s * p.stage_bytes;
-      const uint8_t* codes = st + wide_codes_off(p.Mpad) + r * (WK * BITS / 8) + h * HB;
-      const __half* sc = reinterpret_cast<const __half*>(st + wide_codes_off(p.Mpad) + p.codes_bytes);
+      const uint8_t* codes = st + wide_codes_off(p.chunk) + r * (WK * BITS / 8) + h * HB;
+      const __half* sc = reinterpret_cast<const __half*>(st + wide_codes_off(p.chunk) + p.codes_bytes);
       const __half* bi = sc + WT * 8;
       const float scale = __half2float(sc[r * 8 + (ks & 7)]);
       const float bias = __half2float(bi[r * 8 + (ks & 7)]);
@@ -213,15 +211,15 @@ __global__ void __launch_bounds__(W_THREADS, 1) wide_kernel(const __grid_constan
     tc05_fence_after();
     const int lq = warp & 3;
     const int n = n0 + 32 * lq + lane;
-    const int split_col = (p.Mpad / 32) * 16;  // a multiple of 16: the loads read 16 columns at a time
-    const int col0 = (warp >> 2) ? split_col : 0, col1 = (warp >> 2) ? p.Mpad : split_col;
+    const int split_col = (p.chunk / 32) * 16;  // a multiple of 16: the loads read 16 columns at a time
+    const int col0 = (warp >> 2) ? split_col : 0, col1 = (warp >> 2) ? p.chunk : split_col;
     if (ok) {
       for (int col = col0; col < col1; col += 16) {
         float v[16];
         tmem_ld16(tmem + ((uint32_t)(32 * lq) << 16) + (uint32_t)col, v);
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          const int m = col + j;
+          const int m = m0 + col + j;
           if (m < p.M && n < p.N) {
             const float val = v[j] * p.inv_scale[m];
             if (p.splits > 1) {
@@ -293,18 +291,19 @@ __global__ void __launch_bounds__(256) wide_finish_kernel(const float* __restric
 }
 
 struct WidePlan {
-  int Mpad, nchunk, chunk, stages, splits, tiles, ks_total, stage_bytes, smem;
+  int Mpad, mchunks, chunk, stages, splits, tiles, ks_total, stage_bytes, smem;
   size_t x16, inv, partials, total;
 };
 
 static WidePlan wide_plan(int M, int N, int K, int bits, int sms) {
   WidePlan w;
-  // an MMA takes at most 256 rows (a multiple of 16): wider blocks are two equal chunks
-  w.nchunk = M > 256 ? 2 : 1;
-  w.Mpad = w.nchunk == 1 ? 16 * ((M + 15) / 16) : 32 * ((M + 31) / 32);
-  w.chunk = w.Mpad / w.nchunk;
+  // an MMA takes at most 256 rows (a multiple of 16): wider blocks are two
+  // equal row chunks, each its own CTA
+  w.mchunks = M > 256 ? 2 : 1;
+  w.Mpad = w.mchunks == 1 ? 16 * ((M + 15) / 16) : 32 * ((M + 31) / 32);
+  w.chunk = w.Mpad / w.mchunks;
   const int codes = WT * WK * bits / 8;
-  w.stage_bytes = (wide_codes_off(w.Mpad) + codes + 2 * WT * 16 + 1023) / 1024 * 1024;
+  w.stage_bytes = (wide_codes_off(w.chunk) + codes + 2 * WT * 16 + 1023) / 1024 * 1024;
   const int budget = 226 * 1024 - 1024;  // 1 KB of it aligns the stages
   w.stages = budget / w.stage_bytes;
   if (w.stages > W_MAX_STAGES) w.stages = W_MAX_STAGES;
@@ -312,7 +311,8 @@ static WidePlan wide_plan(int M, int N, int K, int bits, int sms) {
   w.tiles = (N + WT - 1) / WT;
   w.ks_total = K / WK;
   // k splits, in units of the whole GPU's compute time for the projection:
-  // waves of CTAs (sms / tiles * ceil(tiles * s / sms) / s) plus, for s > 1,
+  // waves of CTAs (sms / items * ceil(items * s / sms) / s, items = tiles x
+  // row chunks) plus, for s > 1,
   // the HBM time of writing and re-reading the fp32 partials, which relative
   // to the compute time is about 0.27 * s * 4096 / K (8 B per output per
   // split against 2 K flops per output at this part's bf16 rate and copy
@@ -322,7 +322,8 @@ static WidePlan wide_plan(int M, int N, int K, int bits, int sms) {
     const int max_split = w.ks_total / 8 > 0 ? w.ks_total / 8 : 1;
     double best = 1e30;
     for (int sp = 1; sp <= max_split && sp <= 16; ++sp) {
-      const double waves = (double)sms / w.tiles * (double)((w.tiles * sp + sms - 1) / sms) / sp;
+      const int items = w.tiles * w.mchunks;
+      const double waves = (double)sms / items * (double)((items * sp + sms - 1) / sms) / sp;
       const double cost = waves + (sp > 1 ? 0.27 * sp * 4096.0 / K : 0.0);
       if (cost < best - 1e-12) {
         best = cost;
@@ -390,7 +391,7 @@ int wide_qmm(const uint32_t* wq, const uint16_t* scales, const uint16_t* biases,
   p.K = K;
   p.M = M;
   p.Mpad = w.Mpad;
-  p.nchunk = w.nchunk;
+  p.mchunks = w.mchunks;
   p.chunk = w.chunk;
   p.stages = w.stages;
   p.splits = w.splits;
@@ -398,7 +399,7 @@ int wide_qmm(const uint32_t* wq, const uint16_t* scales, const uint16_t* biases,
   p.stage_bytes = w.stage_bytes;
   p.codes_bytes = WT * WK * bits / 8;
   uint32_t cols = 32;
-  while ((int)cols < w.Mpad) cols <<= 1;
+  while ((int)cols < w.chunk) cols <<= 1;
   p.tmem_cols = cols;
   p.inv_scale = inv;
   p.y = reinterpret_cast<__nv_bfloat16*>(y);
@@ -406,7 +407,7 @@ int wide_qmm(const uint32_t* wq, const uint16_t* scales, const uint16_t* biases,
   p.res = reinterpret_cast<const __nv_bfloat16*>(residual);
   p.ldr = ldr;
   p.partials = w.splits > 1 ? reinterpret_cast<float*>(base + w.partials) : nullptr;
-  const int grid = w.tiles * w.splits;
+  const int grid = w.tiles * w.mchunks * w.splits;
   cudaError_t e = bits == 8 ? launch_wide_t<8>(p, grid, w.smem, s)
                             : (bits == 4 ? launch_wide_t<4>(p, grid, w.smem, s) : launch_wide_t<2>(p, grid, w.smem, s));
   if (e != cudaSuccess) return cuda_fail(e, "wide matmul launch");
