@@ -102,7 +102,6 @@ void stream_params_init(StreamParams& p, void* ws, const Layout& L, int M, int g
   p.act[0] = act_buf(ws, L, 0);
   p.act[1] = L.act[1][0] ? act_buf(ws, L, 1) : p.act[0];
   p.partials = reinterpret_cast<float*>(base + L.partials);
-  p.pair_counters = reinterpret_cast<int*>(base + PAIR_CTR_OFF);
   p.grid_bar = reinterpret_cast<unsigned*>(base + GRID_BAR_OFF);
   p.exit_counter = reinterpret_cast<int*>(base + EXIT_CTR_OFF);
   p.abort_all = reinterpret_cast<int*>(base + ABORT_OFF);

@@ -30,7 +30,7 @@ namespace sv {
 
 struct RoundLayout {
   Layout ws;
-  size_t stats, qkv, gu, total;
+  size_t stats, qkv, gu, pair, total;
   int grid;
 };
 
@@ -45,6 +45,7 @@ static bool round_layout(const sv_model* md, int rows, RoundLayout& R) {
   R.stats = off; off = align256(off + (size_t)rows * 12);
   R.qkv = off;   off = align256(off + (size_t)rows * md->layers[0].qkv.N * 2);
   R.gu = off;    off = align256(off + (size_t)rows * 2 * md->inter * 2);
+  R.pair = off;  off = align256(off + (size_t)((md->inter + BN - 1) / BN) * BN * MP * 4);
   R.total = off;
   return true;
 }
@@ -202,6 +203,7 @@ int sv_verify_round(const sv_model* model, const void* plan, int B, const int32_
   static thread_local StreamParams p;  // about 22 KB: kept off the stack
   stream_params_init(p, workspace, R.ws, M, R.grid, model->rms_eps);
   p.maps = static_cast<const CUtensorMap*>(plan);
+  p.pair_words = reinterpret_cast<float*>(base + R.pair);
   int n = 0;
   for (int l = 0; l < model->n_layers; ++l) {
     const sv_layer& W = model->layers[l];

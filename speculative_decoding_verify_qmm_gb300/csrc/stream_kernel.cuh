@@ -577,24 +577,6 @@ __device__ __forceinline__ int tile_finisher(int tile, int upt, int total, int g
   return unit_owner((long long)tile * upt, total, grid);
 }
 
-// Bounded spin (one thread) until *ctr >= want, with acquire semantics.
-// Returns false on timeout or abort.
-__device__ __forceinline__ bool wait_counter(const int* ctr, int want, volatile int* abort_v, volatile int* abort_g) {
-  const unsigned long long t0 = global_ns();
-  for (unsigned it = 0;; ++it) {
-    if ((int)ld_acquire(reinterpret_cast<const unsigned*>(ctr)) >= want) return true;
-    if ((it & 15u) == 15u) {
-      if (*abort_v | *abort_g) return false;
-      if (global_ns() - t0 > WAIT_LIMIT_NS) {
-        raise_error(ERR_TIMEOUT_FULL);
-        *abort_v = 1;
-        *abort_g = 1;
-        return false;
-      }
-    }
-  }
-}
-
 // Finishes one tile (all four epilogue warps, each holding 16 rows; values are
 // the full sums, before the RMSNorm row factor).  `pre` holds what was fetched
 // before the tile's sums arrived: the hidden-state rows of a PH_RESID tile or
@@ -707,8 +689,7 @@ __device__ void finish_tile(const StreamParams& p, const Phase& ph, const ActBuf
       return;
     }
     if (is_up && !pair_here) {  // the gate tile's finisher (another CTA) combines the pair
-      named_bar_sync(EPI_BAR, EPI_THREADS);
-      if (q == 0 && lane == 0) red_release_add(reinterpret_cast<unsigned*>(p.pair_counters + blk), 1u);
+      partial_store<NT>(p.pair_words + ((size_t)blk * 4 + q) * (16 * MP), yv, lane);
       return;
     }
     // s = bf16(silu(g) * u)
@@ -1060,12 +1041,8 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
           } else if (ph.kind == PH_GATEUP) {
             const int blk = tile >> 1;
             pair_here = tile_finisher(2 * blk, upt, total, pg) == tile_finisher(2 * blk + 1, upt, total, pg);
-            if (!(tile & 1) && !pair_here) {
-              if (q == 0 && lane == 0) wait_counter(p.pair_counters + blk, 1, abort_v, abort_g);
-              named_bar_sync(EPI_BAR, EPI_THREADS);
-              load_tile_bf16<NT>(pre, ph.y, ph.ldy, ph.half + blk * BN, p.M, q, lane);
-              if (q == 0 && lane == 0) p.pair_counters[blk] = 0;
-            }
+            if (!(tile & 1) && !pair_here)  // the up values, published by their finisher as self-announcing words
+              partial_take<NT>(p.pair_words + ((size_t)blk * 4 + q) * C::RED_FLOATS, pre, lane, abort_v, abort_g);
           }
         }
         // ---- the tile's own sums from the consumers

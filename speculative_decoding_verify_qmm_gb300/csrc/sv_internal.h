@@ -31,7 +31,6 @@ enum PrepMode : int { PREP_PLAIN = 0, PREP_RMSNORM = 1, PREP_SWIGLU = 2 };
 constexpr size_t COUNTER_BYTES = 262144;
 constexpr size_t ACC_CTR_OFF = 0;             // the accept step's per-request counters
 constexpr int MAX_TILES = 32768;
-constexpr size_t PAIR_CTR_OFF = 131072;       // per gate/up block pair
 constexpr size_t GRID_BAR_OFF = 196608;       // grid barrier arrivals, one counter per phase transition
 constexpr size_t EXIT_CTR_OFF = 200704;       // CTAs finished
 constexpr size_t ABORT_OFF = 200708;          // some CTA gave up
@@ -72,7 +71,7 @@ struct StreamParams {
   float rms_eps;
   ActBuf act[2];
   float* partials;        // [grid][2 slots][4 quarters][16*MP]
-  int* pair_counters;
+  float* pair_words;      // PH_GATEUP: [blocks][4 quarters][16*MP] up values, self-announcing words
   unsigned* grid_bar;     // [MAX_PHASES]: arrivals for the transition into phase t
   int* exit_counter;
   int* abort_all;
