@@ -1014,6 +1014,20 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
       }
       rms_factors<NT>(in_a, ph.K, lane, rf);
       const int first_tile = u0 / upt, last_tile = (u1 - 1) / upt;
+      // the hidden-state rows of the last residual tile this CTA finishes are
+      // fetched now (h was last written two phases ago): that tile's finish
+      // is at the end of the phase, on its critical path, and would
+      // otherwise wait one L2 round trip for them.  They are held in g_keep,
+      // which carries values only between the two tiles of a gate/up block.
+      int pre_tile = -1;
+      if (ph.kind == PH_RESID) {
+        for (int t = last_tile; t >= first_tile; --t)
+          if (tile_finisher(t, upt, total, pg) == (int)blockIdx.x) {
+            pre_tile = t;
+            break;
+          }
+        if (pre_tile >= 0) load_tile_bf16<NT>(g_keep, ph.res, ph.ldr, pre_tile * BN, p.M, q, lane);
+      }
       for (int tile = first_tile; tile <= last_tile; ++tile) {
         const int fin = tile_finisher(tile, upt, total, pg);
         const int c_last = unit_owner((long long)tile * upt + upt - 1, total, pg);
@@ -1037,7 +1051,14 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
           }
           // ... the hidden-state rows of a residual tile, the partner of a gate tile
           if (ph.kind == PH_RESID) {
-            load_tile_bf16<NT>(pre, ph.res, ph.ldr, tile * BN, p.M, q, lane);
+            if (tile == pre_tile) {
+#pragma unroll
+              for (int j = 0; j < NT; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) pre[j][e] = g_keep[j][e];
+            } else {
+              load_tile_bf16<NT>(pre, ph.res, ph.ldr, tile * BN, p.M, q, lane);
+            }
           } else if (ph.kind == PH_GATEUP) {
             const int blk = tile >> 1;
             pair_here = tile_finisher(2 * blk, upt, total, pg) == tile_finisher(2 * blk + 1, upt, total, pg);
