@@ -29,9 +29,10 @@
 //     then reads them without bank conflicts), one 64 x 8 box each of scales
 //     and biases, and the matching slice of the prepared activations as plain
 //     bulk copies.  The weights run ahead into the next phase while the
-//     current phase drains (at M <= 8 by at most two units: more copies in
-//     flight slow the transition itself); only the activation copies wait
-//     for the grid-wide phase barrier.
+//     current phase drains (by one or two units while the CTA is still
+//     finishing the phase: more copies in flight slow the transition
+//     itself; without a limit once it has arrived at the barrier); only the
+//     activation copies wait for the grid-wide phase barrier.
 //   * warps 0-7 (consumers) are 4 row quarters x 2 k halves: ldmatrix the codes,
 //     turn them into fp16 with byte-permute / LOP3, mma.sync m16n8k16 against
 //     the activation fragments, fold each group into fp32 sums.  At a tile's
@@ -85,10 +86,12 @@ struct StreamCfg {
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + RED_BYTES + EPI_BYTES;
   // units of a phase whose grid barrier has not opened that the weight warp
-  // may copy ahead: more copies in flight while a transition's chain of L2
-  // round trips (split-tile fixup, barrier, first activation copy) runs slow
-  // that chain down by more than they save (measured at M <= 8)
-  static constexpr int RUN_AHEAD = NT == 1 ? RUN_AHEAD_M8 : STAGES;
+  // may copy ahead while this CTA is still finishing the previous phase:
+  // more copies in flight then slow the transition's chain of L2 round trips
+  // (split-tile fixup, barrier, first activation copy) by more than they
+  // save.  Once the CTA has arrived at the barrier the ring fills without a
+  // limit (measured best: 2 units at M <= 8, 1 above).
+  static constexpr int RUN_AHEAD = NT == 1 ? RUN_AHEAD_M8 : 1;
   static_assert(STAGES >= 2, "stage ring too small");
   static_assert(SMEM + 2048 <= 227 * 1024, "shared memory budget");
   static_assert(W_BYTES % 1024 == 0 && X_OFF % 16 == 0 && XS_OFF % 16 == 0 && S_OFF % 128 == 0 &&
@@ -778,6 +781,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
   __shared__ uint64_t full_bar[S], empty_bar[S], res_full[2], res_empty[2];
   __shared__ int abort_flag;
   __shared__ int ready_ph;             // highest phase whose grid barrier the producer passed
+  __shared__ int arrived_ph;           // highest phase this CTA's epilogue has finished (arrived for)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* red = reinterpret_cast<float*>(smem + S * C::STAGE_BYTES);  // result slots [2][4][16*MP]
   float* epi = red + 2 * 4 * C::RED_FLOATS;
@@ -802,6 +806,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
     }
     abort_flag = 0;
     ready_ph = 0;
+    arrived_ph = -1;
     fence_mbar_init();
   }
   __syncthreads();
@@ -842,7 +847,8 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
       bool go = false;
       // the stage must be free: its previous unit consumed
       bool free_slot = n < S || mbar_test_wait(&empty_bar[n % S], ((n / S) - 1) & 1);
-      if (free_slot && !is_x && it.phase > ld_acquire_cta(&ready_ph)) {
+      if (free_slot && !is_x && it.phase > ld_acquire_cta(&ready_ph) &&
+          it.phase > ld_acquire_cta(&arrived_ph) + 1) {
         if (ahead_ph != it.phase) {
           ahead_ph = it.phase;
           ahead_n = 0;
@@ -1100,6 +1106,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
     fence_proxy_async();
     named_bar_sync(EPI_BAR, EPI_THREADS);
     if (q == 0 && lane == 0 && ph_i + 1 < p.n_phases) red_release_add(p.grid_bar + ph_i + 1, 1u);
+    if (q == 0 && lane == 0) st_release_cta(&arrived_ph, ph_i);  // the weights may now fill the ring
   }
   named_bar_sync(6, NEW * 32);  // every arrival of this CTA is made
   // the last CTA to finish resets the grid counters (the workspace's counters
