@@ -43,7 +43,7 @@ __global__ void __launch_bounds__(256) swiglu_kernel(const __nv_bfloat16* g, int
   for (int k = blockIdx.x * 256 + threadIdx.x; k < I; k += gridDim.x * 256) {
     const float gv = __bfloat162float(g[(size_t)m * ldg + k]);
     const float uv = __bfloat162float(u[(size_t)m * ldu + k]);
-    out[(size_t)m * lds + k] = __float2bfloat16_rn(gv / (1.f + expf(-gv)) * uv);
+    out[(size_t)m * lds + k] = __float2bfloat16_rn(silu_f32(gv) * uv);
   }
 }
 

@@ -583,10 +583,13 @@ __device__ __forceinline__ int tile_finisher(int tile, int upt, int total, int g
 // Finishes one tile (all four epilogue warps, each holding 16 rows; values are
 // the full sums, before the RMSNorm row factor).  `pre` holds what was fetched
 // before the tile's sums arrived: the hidden-state rows of a PH_RESID tile or
-// the partner up values of a gate tile whose up half another CTA finished.
+// the partner up values of a gate tile whose up half another CTA finished,
+// or the gate values of an up tile whose gate half this CTA finished.
 // `g_keep` carries a gate tile's values to its up tile when one CTA finishes
-// both (`pair_here`); otherwise the up tile's finisher publishes its values and
-// the gate tile's finisher, which meets its tile later, combines the two.
+// both (`pair_here`; they are copied to `pre` before the up tile's sums
+// arrive, so that a register spill of `g_keep` is not reloaded in the tail);
+// otherwise the up tile's finisher publishes its values and the gate tile's
+// finisher, which meets its tile later, combines the two.
 template <int BITS, int NT>
 __device__ void finish_tile(const StreamParams& p, const Phase& ph, const ActBuf& out, int tile, int pair_here, int q, int lane,
                             float (&tot)[NT][4], const float (&rf)[NT][2], const float (&pre)[NT][4],
@@ -701,9 +704,9 @@ __device__ void finish_tile(const StreamParams& p, const Phase& ph, const ActBuf
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int m = 8 * j + 2 * t + (e & 1);
-        const float g = is_up ? g_keep[j][e] : yv[j][e];
+        const float g = is_up ? pre[j][e] : yv[j][e];  // an up tile's pre holds its gate values
         const float u = is_up ? yv[j][e] : pre[j][e];
-        yv[j][e] = m < p.M ? __bfloat162float(__float2bfloat16_rn(g / (1.f + expf(-g)) * u)) : 0.f;
+        yv[j][e] = m < p.M ? __bfloat162float(__float2bfloat16_rn(silu_f32(g) * u)) : 0.f;
       }
     prepare_group<BITS, NT>(p, out, blk, ph.half, q, lane, yv, false, -1.f, es);
     return;
@@ -1070,6 +1073,12 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
             pair_here = tile_finisher(2 * blk, upt, total, pg) == tile_finisher(2 * blk + 1, upt, total, pg);
             if (!(tile & 1) && !pair_here)  // the up values, published by their finisher as self-announcing words
               partial_take<NT>(p.pair_words + ((size_t)blk * 4 + q) * C::RED_FLOATS, pre, lane, abort_v, abort_g);
+            if ((tile & 1) && pair_here) {  // the gate values this CTA kept, read back before the sums arrive
+#pragma unroll
+              for (int j = 0; j < NT; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) pre[j][e] = g_keep[j][e];
+            }
           }
         }
         // ---- the tile's own sums from the consumers

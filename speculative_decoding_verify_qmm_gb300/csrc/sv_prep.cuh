@@ -40,7 +40,7 @@ __device__ __forceinline__ void prep_group(const __nv_bfloat16* row, const __nv_
         if (w) x = __bfloat162float(__float2bfloat16_rn(x * __bfloat162float(w[k])));
       } else if (MODE == PREP_SWIGLU) {
         const float u = __bfloat162float(row2[k]);
-        x = __bfloat162float(__float2bfloat16_rn(x / (1.f + expf(-x)) * u));
+        x = __bfloat162float(__float2bfloat16_rn(silu_f32(x) * u));
       }
       v[i] = x;
     }
