@@ -499,22 +499,14 @@ __device__ void prepare_group(const StreamParams& p, const ActBuf& out, int grp,
     }
   named_bar_sync(EPI_BAR, EPI_THREADS);
   // 2. exponent per column, scaled fp16 values, partial group sums
-  float sc[NT][2], inv[NT][2];
+  float sc[NT][2];
 #pragma unroll
   for (int j = 0; j < NT; ++j)
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
       const int m = 8 * j + 2 * t + c;
-      const float mx = fmaxf(fmaxf(es.a[m], es.a[MP + m]), fmaxf(es.a[2 * MP + m], es.a[3 * MP + m]));
-      int e = 0;
-      if (mx > 0.f && mx <= 3.0e38f) {
-        int E;
-        frexpf(mx, &E);
-        e = 15 - E;
-        e = e > 100 ? 100 : (e < -100 ? -100 : e);
-      }
-      sc[j][c] = ldexpf(1.f, e);
-      inv[j][c] = ldexpf(1.f, -e);
+      const int e = scale_exponent(fmaxf(fmaxf(es.a[m], es.a[MP + m]), fmaxf(es.a[2 * MP + m], es.a[3 * MP + m])));
+      sc[j][c] = pow2_exact(e);
     }
   const int n_lo = 16 * q + gid, n_hi = n_lo + 8;
   __half* xp = out.xp;
@@ -536,22 +528,14 @@ __device__ void prepare_group(const StreamParams& p, const ActBuf& out, int grp,
   // 3. one warp writes the group's sums (fixed quarter order)
   if (q == 0) {
     for (int m = lane; m < MP; m += 32) {
-      const float mx = fmaxf(fmaxf(es.a[m], es.a[MP + m]), fmaxf(es.a[2 * MP + m], es.a[3 * MP + m]));
-      int e = 0;
-      if (mx > 0.f && mx <= 3.0e38f) {
-        int E;
-        frexpf(mx, &E);
-        e = 15 - E;
-        e = e > 100 ? 100 : (e < -100 ? -100 : e);
-      }
+      const int e = scale_exponent(fmaxf(fmaxf(es.a[m], es.a[MP + m]), fmaxf(es.a[2 * MP + m], es.a[3 * MP + m])));
       float* xs = out.xs + (size_t)grp * 2 * MP;
       xs[m] = ((es.c[m] + es.c[MP + m]) + es.c[2 * MP + m]) + es.c[3 * MP + m];
-      xs[MP + m] = ldexpf(1.f, -e);
+      xs[MP + m] = pow2_exact(-e);
       if (with_sq) out.sq[(size_t)grp * MP + m] = ((es.b[m] + es.b[MP + m]) + es.b[2 * MP + m]) + es.b[3 * MP + m];
       if (grp == 0) out.sq[(size_t)(Kn / GROUP) * MP + m] = flag_value;
     }
   }
-  (void)inv;
   named_bar_sync(EPI_BAR, EPI_THREADS);
 }
 

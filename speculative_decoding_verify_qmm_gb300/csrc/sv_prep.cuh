@@ -50,14 +50,8 @@ __device__ __forceinline__ void prep_group(const __nv_bfloat16* row, const __nv_
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
     sq += __shfl_xor_sync(0xffffffffu, sq, off);
   }
-  int e = 0;
-  if (mx > 0.f && mx <= 3.0e38f) {
-    int E;
-    frexpf(mx, &E);  // mx = f * 2^E, f in [0.5, 1)
-    e = 15 - E;
-    e = e > 100 ? 100 : (e < -100 ? -100 : e);
-  }
-  const float sc = ldexpf(1.f, e);
+  const int e = scale_exponent(mx);
+  const float sc = pow2_exact(e);
   float gs = 0.f;
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
@@ -70,7 +64,7 @@ __device__ __forceinline__ void prep_group(const __nv_bfloat16* row, const __nv_
   if (lane == 0) {
     float* xs = out.xs + (size_t)g * 2 * MP;
     xs[m] = gs;
-    xs[MP + m] = ldexpf(1.f, -e);
+    xs[MP + m] = pow2_exact(-e);
     out.sq[(size_t)g * MP + m] = sq;
     if (g == 0) out.sq[(size_t)(K / GROUP) * MP + m] = MODE == PREP_RMSNORM ? eps : -1.f;
   }

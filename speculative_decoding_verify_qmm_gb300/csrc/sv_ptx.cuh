@@ -176,6 +176,19 @@ __device__ __forceinline__ int ld_acquire_cta(const int* addr) {
 // Order this thread's generic-proxy global writes before later async-proxy (bulk copy) reads.
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
+// Scale exponent of a block of activations with largest magnitude mx: e =
+// 15 - E where mx = f * 2^E, f in [0.5, 1) (so mx * 2^e lies in [2^14, 2^15)),
+// clamped to [-100, 100]; 0 when mx is zero, not finite or above 3e38.  Read
+// off the exponent field: for a normal mx the field b gives E = b - 126; a
+// subnormal mx gives at most -126 either way, and e is clamped at 100 then.
+__device__ __forceinline__ int scale_exponent(float mx) {
+  if (!(mx > 0.f && mx <= 3.0e38f)) return 0;
+  const int e = 15 - ((int)((__float_as_uint(mx) >> 23) & 0xFFu) - 126);
+  return e > 100 ? 100 : (e < -100 ? -100 : e);
+}
+// 2^e as an exact fp32 value for -126 <= e <= 127.
+__device__ __forceinline__ float pow2_exact(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
+
 // silu(g) = g / (1 + exp(-g)) in fp32, in a form whose intermediates stay
 // normal: e = exp(-|g|) lies in [0, 1], the divisor 1 + e in [1, 2], and for
 // g < 0 the numerator is g * e (the same value: g / (1 + exp(-g)) =

@@ -260,17 +260,11 @@ __global__ void __launch_bounds__(256) wide_prep_kernel(const __nv_bfloat16* __r
   __syncthreads();
   mx = 0.f;
   for (int w = 0; w < 8; ++w) mx = fmaxf(mx, s_max[w]);
-  int e = 0;
-  if (mx > 0.f && mx <= 3.0e38f) {
-    int E;
-    frexpf(mx, &E);
-    e = 15 - E;
-    e = e > 100 ? 100 : (e < -100 ? -100 : e);
-  }
-  const float sc = ldexpf(1.f, e);
+  const int e = scale_exponent(mx);
+  const float sc = pow2_exact(e);
   for (int k = tid; k < K; k += 256)
     x16[(size_t)m * K + k] = __float2half_rn(m < M ? __bfloat162float(x[(size_t)m * ldx + k]) * sc : 0.f);
-  if (tid == 0) inv[m] = ldexpf(1.f, -e);
+  if (tid == 0) inv[m] = pow2_exact(-e);
 }
 
 // Sum of the split partials in split order, then bf16 (with the optional residual).
