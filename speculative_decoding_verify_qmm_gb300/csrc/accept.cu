@@ -123,6 +123,11 @@ __global__ void __launch_bounds__(ACC_THREADS) accept_kernel(const AcceptParams 
   const float zmax = p.row_max[row], S = trunc ? p.tnorm[row] : p.row_sumexp[row], T = p.temperature;
   const uint32_t tK = trunc ? p.tkey[row] : 0u;
   const int tI = trunc ? p.tidx[row] : V;
+  // p_k = exp((z_k - zmax) / T) / S with the two divisions as products by
+  // reciprocals taken once (a few fp32 ulps, far below the draw's 1e-6 Z
+  // exemption) and vanishing terms set to 0: every element of the vocabulary
+  // passes through here, and the IEEE forms took slow paths on most of them
+  const float inv_t = 1.f / T, inv_s = 1.f / S;
   auto weight = [&](int k, float& pk) -> float {
     const float zk = z[k];
     bool kept = true;
@@ -130,7 +135,7 @@ __global__ void __launch_bounds__(ACC_THREADS) accept_kernel(const AcceptParams 
       const uint32_t key = order_key(zk);
       kept = key > tK || (key == tK && k <= tI);
     }
-    pk = kept ? expf((zk - zmax) / T) / S : 0.f;
+    pk = kept ? exp_term((zk - zmax) * inv_t) * inv_s : 0.f;
     return resid ? fmaxf(0.f, pk - qr[k]) : pk;
   };
 
@@ -325,7 +330,7 @@ __global__ void __launch_bounds__(1024) row_stats_kernel(const float* __restrict
   bi = si[0];
   if (temperature > 0.f) {
     double acc = 0.0;
-    for (int k = tid; k < V; k += 1024) acc += (double)expf((z[k] - best) / temperature);
+    for (int k = tid; k < V; k += 1024) acc += (double)exp_term((z[k] - best) / temperature);
     sd[tid] = acc;
     __syncthreads();
     for (int w = 512; w; w >>= 1) {

@@ -105,7 +105,7 @@ __global__ void __launch_bounds__(256) lmhead_finalize_kernel(const float* __res
     for (int t = tid; t < tiles; t += 256) {
       const float v = ts[((size_t)t * MP + m) * 3];
       const float se = ts[((size_t)t * MP + m) * 3 + 2];
-      acc += (double)(se * expf((v - best) * inv_temp));
+      acc += (double)(se * exp_term((v - best) * inv_temp));
     }
     sd[tid] = acc;
     __syncthreads();

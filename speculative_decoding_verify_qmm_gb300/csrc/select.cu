@@ -169,7 +169,7 @@ __global__ void __launch_bounds__(SEL_THREADS) select_kernel(const SelectArgs p)
     }
   }
   // a token's weight: exp((z - max) / T) exactly as the accept step computes it, or the probability
-  auto weight = [&](float xv) -> double { return probs ? (double)xv : (double)expf((xv - xmax) / T); };
+  auto weight = [&](float xv) -> double { return probs ? (double)xv : (double)exp_term((xv - xmax) / T); };
 
   // ---- top-k: the k-th key in the order (by counts), then its tie index
   const int k_lim = p.mode == SEL_TOPN ? min(p.top_n, V) : p.top_k;

@@ -633,7 +633,7 @@ __device__ void finish_tile(const StreamParams& p, const Phase& ph, const ActBuf
         if (p.inv_temp > 0.f) {
 #pragma unroll
           for (int h = 0; h < 2; ++h)
-            if (n_lo + 8 * h < ph.N) se += expf((yv[j][2 * h + c] - best) * p.inv_temp);
+            if (n_lo + 8 * h < ph.N) se += exp_term((yv[j][2 * h + c] - best) * p.inv_temp);
 #pragma unroll
           for (int off = 4; off < 32; off <<= 1) se += __shfl_xor_sync(0xffffffffu, se, off);
         }

@@ -176,6 +176,11 @@ __device__ __forceinline__ int ld_acquire_cta(const int* addr) {
 // Order this thread's generic-proxy global writes before later async-proxy (bulk copy) reads.
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
+// exp(x) for x <= 0 as a term of a softmax sum or a draw weight (the maximum
+// term is 1): x <= -87 gives 0 instead of a result below 1.2e-38, which keeps
+// expf (and anything dividing its result) off the subnormal slow paths.
+__device__ __forceinline__ float exp_term(float x) { return x > -87.f ? expf(x) : 0.f; }
+
 // Scale exponent of a block of activations with largest magnitude mx: e =
 // 15 - E where mx = f * 2^E, f in [0.5, 1) (so mx * 2^e lies in [2^14, 2^15)),
 // clamped to [-100, 100]; 0 when mx is zero, not finite or above 3e38.  Read
