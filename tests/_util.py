@@ -45,16 +45,17 @@ def bf16_ulp(x):
     return np.where(a > 0, 2.0 ** (e - 7), 0.0)
 
 
-def assert_close_bf16(got, want, tol=REL_TOL, what=""):
+def assert_close_bf16(got, want, tol=REL_TOL, what="", ulps=1):
     """Parity of bf16 outputs.  Each side rounds its fp32-accumulated value to
     bf16 once; the REL_TOL * rms rule bounds the accumulation error, and one
     bf16 ulp at the element's magnitude covers a rounding that falls on the
-    other side of a bf16 boundary."""
+    other side of a bf16 boundary (`ulps` such roundings for a value that
+    passes through several bf16 results in turn)."""
     got = np.asarray(got, dtype=np.float64)
     want = np.asarray(want, dtype=np.float64)
     assert got.shape == want.shape, (got.shape, want.shape)
     rms = np.sqrt(np.mean(want ** 2))
-    excess = np.abs(got - want) - bf16_ulp(want)
+    excess = np.abs(got - want) - ulps * bf16_ulp(want)
     err = excess.max() if got.size else 0.0
     assert err <= tol * rms, "%s max err beyond one bf16 ulp %.3e > %.1e * rms %.3e" % (what, err, tol, rms)
     return err / rms if rms else 0.0

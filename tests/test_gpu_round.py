@@ -235,7 +235,8 @@ def test_qwen3_8b_round_per_layer_and_head(lib, model_8b, M, T):
         after, logits, n, toks = run(depth)
         lay = _model.split_device_layer(layers[depth - 1], QWEN8B["q_dim"], QWEN8B["kv_dim"], QWEN8B["inter"])
         want = chain.layer_forward(before, lay)
-        assert_close_bf16(host_f32_of_bf16(after), quant.bf16_bits_to_f32(want), what="layer %d" % depth)
+        # the hidden state is rounded to bf16 twice in a layer (h + o, then + down)
+        assert_close_bf16(host_f32_of_bf16(after), quant.bf16_bits_to_f32(want), what="layer %d" % depth, ulps=2)
     # vocab head on sampled rows, from the GPU's final hidden state
     lg = logits.cpu().numpy()
     rows = np.unique(np.concatenate([r.choice(QWEN8B["vocab"], 2048, replace=False), np.argmax(lg, axis=1)]))
@@ -271,7 +272,8 @@ def _check_round_layers(lib, layers, head, shape, offs, h0, T, depths, q=None, d
         after, logits, n, toks = run(depth)
         lay = _model.split_device_layer(layers[depth - 1], shape["q_dim"], shape["kv_dim"], shape["inter"])
         want = chain.layer_forward(before, lay)
-        assert_close_bf16(host_f32_of_bf16(after), quant.bf16_bits_to_f32(want), what="layer %d" % depth)
+        # the hidden state is rounded to bf16 twice in a layer (h + o, then + down)
+        assert_close_bf16(host_f32_of_bf16(after), quant.bf16_bits_to_f32(want), what="layer %d" % depth, ulps=2)
     lg = logits.cpu().numpy()
     rows = np.unique(np.concatenate([r.choice(shape["vocab"], 2048, replace=False), np.argmax(lg, axis=1)]))
     hw = _model.host_copy(head)
