@@ -80,7 +80,7 @@ struct StreamCfg {
   static constexpr int STAGE_BYTES = (XS_OFF + XS_BYTES + 1023) / 1024 * 1024;  // swizzle atoms 1024-aligned
   static constexpr int RED_FLOATS = 16 * MP;        // one quarter's 16 rows
   static constexpr int RED_BYTES = 2 * 4 * RED_FLOATS * 4;  // result slot x quarter
-  static constexpr int EPI_BYTES = 4 * 4 * MP * 4 + 256;    // cross-quarter scratch
+  static constexpr int EPI_BYTES = 5 * 4 * MP * 4 + 256;    // cross-quarter scratch
   static constexpr int BUDGET = 227 * 1024 - 1024 - 2048 - RED_BYTES - EPI_BYTES;
   static constexpr int STAGES_FIT = BUDGET / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
@@ -468,7 +468,7 @@ struct EpiScratch {
   float* b;    // [4][MP]
   float* c;    // [4][MP]
   int* ia;     // [4][MP] (aliases c for the argmax)
-  int* flag;   // one int
+  float* r;    // [4][MP]: RMSNorm sums of squares, one part per epilogue warp
 };
 
 // Turns this tile's 64 output columns (row values yv, already final) into group
@@ -732,27 +732,42 @@ __device__ void finish_tile(const StreamParams& p, const Phase& ph, const ActBuf
 }
 
 // RMSNorm row factors 1/sqrt(mean(x^2) + eps) of the phase input for this
-// thread's columns, or 1 when the input is not an RMSNorm input.  The warp
-// shares the work: LPC lanes per column each sum every LPC-th group of that
-// column, then a fixed shuffle tree adds them.
+// thread's columns, or 1 when the input is not an RMSNorm input.  The four
+// epilogue warps split the groups into four contiguous ranges; in each, LPC
+// lanes per column sum every LPC-th group with eight loads in flight, a fixed
+// shuffle tree adds the lanes, and the four parts are added in warp order
+// through shared memory (all four warps call this together).
 template <int NT>
-__device__ __forceinline__ void rms_factors(const ActBuf& a, int K, int lane, float (&rf)[NT][2]) {
+__device__ __forceinline__ void rms_factors(const ActBuf& a, int K, int q, int lane, float (&rf)[NT][2], float* part_sums) {
   constexpr int MP = 8 * NT;
   constexpr int LPC = MP == 8 ? 4 : (MP == 16 ? 2 : 1);  // MP = 24: lanes 24..31 idle
   const int G = K / GROUP;
   const float eps = __ldcg(a.sq + (size_t)G * MP);
-  if (!(eps >= 0.f)) {
+  if (!(eps >= 0.f)) {  // the same word for every warp: all take this branch or none
 #pragma unroll
     for (int j = 0; j < NT; ++j) rf[j][0] = rf[j][1] = 1.f;
     return;
   }
   const int m = lane % MP, part = lane / MP;
+  const int g0 = q * G / 4, g1 = (q + 1) * G / 4;
   float ss = 0.f;
-  if (part < LPC)
-    for (int g = part; g < G; g += LPC) ss += __ldcg(a.sq + (size_t)g * MP + m);
+  if (part < LPC) {
+    int g = g0 + part;
+    for (; g + 7 * LPC < g1; g += 8 * LPC) {
+      float v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = __ldcg(a.sq + (size_t)(g + i * LPC) * MP + m);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ss += v[i];
+    }
+    for (; g < g1; g += LPC) ss += __ldcg(a.sq + (size_t)g * MP + m);
+  }
 #pragma unroll
   for (int off = MP; off < MP * LPC; off <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-  const float r_mine = 1.f / sqrtf(ss / (float)K + eps);
+  if (lane < MP) part_sums[q * MP + lane] = ss;
+  named_bar_sync(EPI_BAR, EPI_THREADS);
+  const float tot = ((part_sums[m] + part_sums[MP + m]) + part_sums[2 * MP + m]) + part_sums[3 * MP + m];
+  const float r_mine = 1.f / sqrtf(tot / (float)K + eps);
 #pragma unroll
   for (int j = 0; j < NT; ++j)
 #pragma unroll
@@ -777,7 +792,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
   es.b = epi + 4 * MP;
   es.c = epi + 8 * MP;
   es.ia = reinterpret_cast<int*>(epi + 12 * MP);
-  es.flag = reinterpret_cast<int*>(epi + 16 * MP);
+  es.r = epi + 16 * MP;
   volatile int* abort_v = &abort_flag;
   volatile int* abort_g = p.abort_all;
 
@@ -1005,7 +1020,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) stream_kernel(const __grid_con
           __nanosleep(32);
         }
       }
-      rms_factors<NT>(in_a, ph.K, lane, rf);
+      rms_factors<NT>(in_a, ph.K, q, lane, rf, es.r);
       const int first_tile = u0 / upt, last_tile = (u1 - 1) / upt;
       // the hidden-state rows of the last residual tile this CTA finishes are
       // fetched now (h was last written two phases ago): that tile's finish
