@@ -23,6 +23,7 @@ namespace sv {
 
 constexpr int ACC_THREADS = 256;
 constexpr int ACC_CACHE = 8192;  // vocabulary chunk held in shared memory by the drawing CTA
+constexpr int ACC_BATCH = 10;    // vocabulary elements per thread whose loads are in flight together
 
 // Warp reductions and scans in a fixed order (shuffle trees), so every run
 // adds the same values in the same order.
@@ -143,18 +144,18 @@ __global__ void __launch_bounds__(ACC_THREADS) accept_kernel(const AcceptParams 
   const int NB = p.nb;
   const int k0 = (int)((long long)chunk * V / NB), k1 = (int)((long long)(chunk + 1) * V / NB);
   float sw = 0.f, sp = 0.f;  // at most a few dozen terms per thread: fp32 holds them to ~1e-7
-  // four elements per turn with their loads issued together (the loop is
-  // latency-bound: every element is a load from L2)
-  for (int k = k0 + tid; k < k1; k += 4 * ACC_THREADS) {
-    float wk[4], pk[4];
+  // ACC_BATCH elements per turn with their loads issued together (the loop
+  // is latency-bound: every element is a load from L2)
+  for (int k = k0 + tid; k < k1; k += ACC_BATCH * ACC_THREADS) {
+    float wk[ACC_BATCH], pk[ACC_BATCH];
 #pragma unroll
-    for (int v = 0; v < 4; ++v) {
+    for (int v = 0; v < ACC_BATCH; ++v) {
       const int kk = k + v * ACC_THREADS;
       wk[v] = pk[v] = 0.f;
       if (kk < k1) wk[v] = weight(kk, pk[v]);
     }
 #pragma unroll
-    for (int v = 0; v < 4; ++v) {
+    for (int v = 0; v < ACC_BATCH; ++v) {
       sw += wk[v];
       sp += pk[v];
     }
@@ -224,17 +225,17 @@ __global__ void __launch_bounds__(ACC_THREADS) accept_kernel(const AcceptParams 
   // shared memory; each thread then sums its contiguous sub-range
   const bool cached = len <= ACC_CACHE;
   if (cached) {
-    for (int k = c0 + tid; k < c1; k += 4 * ACC_THREADS) {
-      float wv[4];
+    for (int k = c0 + tid; k < c1; k += ACC_BATCH * ACC_THREADS) {
+      float wv[ACC_BATCH];
 #pragma unroll
-      for (int v = 0; v < 4; ++v) {
+      for (int v = 0; v < ACC_BATCH; ++v) {
         const int kk = k + v * ACC_THREADS;
         float pk = 0.f, wk = 0.f;
         if (kk < c1) wk = weight(kk, pk);
         wv[v] = from_p ? pk : wk;
       }
 #pragma unroll
-      for (int v = 0; v < 4; ++v)
+      for (int v = 0; v < ACC_BATCH; ++v)
         if (k + v * ACC_THREADS < c1) s_cache[k + v * ACC_THREADS - c0] = wv[v];
     }
     __syncthreads();

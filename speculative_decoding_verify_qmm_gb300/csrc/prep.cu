@@ -68,63 +68,97 @@ cudaError_t launch_prep(const PrepArgs& a, int bits, int mode, cudaStream_t s) {
 }
 
 // One block per row: merge the per-slice (max, argmax, sumexp) triples of the
-// 32-column slices in order.  Ties keep the lowest vocabulary index; each
-// slice's sum-exp is rescaled to the global maximum (fp32 exp of a
-// non-positive argument) and the terms are added in fp64 in a fixed order.
-__global__ void __launch_bounds__(256) lmhead_finalize_kernel(const float* __restrict__ ts, int tiles, int MP,
-                                                              float inv_temp, float* row_max, float* row_sumexp,
-                                                              int32_t* row_argmax) {
+// 64-column tiles.  Ties keep the lowest vocabulary index; each tile's sum-exp
+// is rescaled to the global maximum (fp32 exp of a non-positive argument) and
+// the terms are added in fp64 in a fixed order (each thread its tiles in
+// order, then the lanes of a warp by a shuffle tree, then the warps in order).
+// A thread loads its tiles FIN_PT at a time, together (each load is an L2
+// round trip), and a row of at most FIN_PT * FIN_THREADS tiles stays in
+// registers for both passes.
+constexpr int FIN_THREADS = 256, FIN_PT = 16, FIN_CHUNK = FIN_PT * FIN_THREADS;
+__global__ void __launch_bounds__(FIN_THREADS) lmhead_finalize_kernel(const float* __restrict__ ts, int tiles, int MP,
+                                                                      float inv_temp, float* row_max,
+                                                                      float* row_sumexp, int32_t* row_argmax) {
   pdl_trigger();
   pdl_wait();
-  const int m = blockIdx.x, tid = threadIdx.x;
-  __shared__ float sb[256];
-  __shared__ int si[256];
-  __shared__ double sd[256];
+  const int m = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  __shared__ float s_best[FIN_THREADS / 32];
+  __shared__ int s_idx[FIN_THREADS / 32];
+  __shared__ double s_sum[FIN_THREADS / 32];
+  __shared__ float s_row_best;
+  float v[FIN_PT], se[FIN_PT];
+  auto load = [&](int base) {  // tiles base + tid + k * FIN_THREADS; returns their lowest-index maximum
+    float b = -INFINITY;
+    int bi = 0x7fffffff;
+    int ix[FIN_PT];
+#pragma unroll
+    for (int k = 0; k < FIN_PT; ++k) {
+      const int t = base + tid + k * FIN_THREADS;
+      v[k] = -INFINITY;
+      se[k] = 0.f;
+      ix[k] = 0x7fffffff;
+      if (t < tiles) {
+        const float* e = ts + ((size_t)t * MP + m) * 3;
+        v[k] = e[0];
+        ix[k] = __float_as_int(e[1]);
+        se[k] = e[2];
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < FIN_PT; ++k)
+      if (v[k] > b || (v[k] == b && ix[k] < bi)) { b = v[k]; bi = ix[k]; }
+    return make_float2(b, __int_as_float(bi));
+  };
   float best = -INFINITY;
   int bi = 0x7fffffff;
-  for (int t = tid; t < tiles; t += 256) {
-    const float v = ts[((size_t)t * MP + m) * 3];
-    const int i = __float_as_int(ts[((size_t)t * MP + m) * 3 + 1]);
-    if (v > best || (v == best && i < bi)) { best = v; bi = i; }
+  for (int base = 0; base < tiles; base += FIN_CHUNK) {
+    const float2 r = load(base);
+    const int ri = __float_as_int(r.y);
+    if (r.x > best || (r.x == best && ri < bi)) { best = r.x; bi = ri; }
   }
-  sb[tid] = best;
-  si[tid] = bi;
+#pragma unroll
+  for (int off = 16; off; off >>= 1) {
+    const float ob = __shfl_xor_sync(0xffffffffu, best, off);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+    if (ob > best || (ob == best && oi < bi)) { best = ob; bi = oi; }
+  }
+  if (lane == 0) {
+    s_best[wid] = best;
+    s_idx[wid] = bi;
+  }
   __syncthreads();
-  for (int w = 128; w; w >>= 1) {
-    if (tid < w) {
-      const float ob = sb[tid + w];
-      const int oi = si[tid + w];
-      if (ob > sb[tid] || (ob == sb[tid] && oi < si[tid])) { sb[tid] = ob; si[tid] = oi; }
-    }
-    __syncthreads();
-  }
-  best = sb[0];
-  bi = si[0];
-  if (inv_temp > 0.f) {
-    double acc = 0.0;
-    for (int t = tid; t < tiles; t += 256) {
-      const float v = ts[((size_t)t * MP + m) * 3];
-      const float se = ts[((size_t)t * MP + m) * 3 + 2];
-      acc += (double)(se * exp_term((v - best) * inv_temp));
-    }
-    sd[tid] = acc;
-    __syncthreads();
-    for (int w = 128; w; w >>= 1) {
-      if (tid < w) sd[tid] += sd[tid + w];
-      __syncthreads();
-    }
-  }
   if (tid == 0) {
+    for (int w = 1; w < FIN_THREADS / 32; ++w)
+      if (s_best[w] > best || (s_best[w] == best && s_idx[w] < bi)) { best = s_best[w]; bi = s_idx[w]; }
+    s_row_best = best;
     if (row_max) row_max[m] = best;
     if (row_argmax) row_argmax[m] = bi;
-    if (row_sumexp && inv_temp > 0.f) row_sumexp[m] = (float)sd[0];
+  }
+  __syncthreads();
+  if (!(inv_temp > 0.f)) return;
+  best = s_row_best;
+  double acc = 0.0;
+  for (int base = 0; base < tiles; base += FIN_CHUNK) {
+    if (tiles > FIN_CHUNK) load(base);  // a single chunk is still in registers
+#pragma unroll
+    for (int k = 0; k < FIN_PT; ++k)
+      if (base + tid + k * FIN_THREADS < tiles) acc += (double)(se[k] * exp_term((v[k] - best) * inv_temp));
+  }
+#pragma unroll
+  for (int off = 16; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) s_sum[wid] = acc;
+  __syncthreads();
+  if (tid == 0) {
+    double tot = 0.0;
+    for (int w = 0; w < FIN_THREADS / 32; ++w) tot += s_sum[w];
+    if (row_sumexp) row_sumexp[m] = (float)tot;
   }
 }
 
 cudaError_t launch_lmhead_finalize(const float* tile_stats, int tiles_n, int MP, int M, float inv_temp,
                                    float* row_max, float* row_sumexp, int32_t* row_argmax, cudaStream_t s) {
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = pdl_config(dim3(M), dim3(256), 0, s, attr);
+  cudaLaunchConfig_t cfg = pdl_config(dim3(M), dim3(FIN_THREADS), 0, s, attr);
   return cudaLaunchKernelEx(&cfg, lmhead_finalize_kernel, tile_stats, tiles_n, MP, inv_temp, row_max, row_sumexp,
                             row_argmax);
 }
