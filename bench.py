@@ -357,6 +357,14 @@ def batched_27b(lib, steps, warmup, hbm):
     return out
 
 
+# single projections of the one-layer 8B sweep and the tiny 4-bit layer:
+# name -> (N, K, bits, the row counts timed)
+PROJ_SHAPES = {"8b_" + name: (N, K, 8, (1, 2, 4, 6, 8, 12, 16, 17))
+               for name, (N, K) in {"q": (4096, 4096), "k": (1024, 4096), "o": (4096, 4096),
+                                    "gate": (12288, 4096), "down": (4096, 12288)}.items()}
+PROJ_SHAPES["tiny_4bit_1024"] = (1024, 1024, 4, (1, 2, 4, 8))
+
+
 def projections(lib, steps, warmup, hbm):
     """Single projections through sv_qmm_verify, rotating weight copies that
     together exceed 2 x L2, so every call streams its weights from HBM."""
@@ -386,10 +394,9 @@ def projections(lib, steps, warmup, hbm):
         out[name] = {"N": N, "K": K, "bits": bits, "copies_rotated": copies, "by_M": res}
         del ws
 
-    for name, (N, K) in {"q": (4096, 4096), "k": (1024, 4096), "o": (4096, 4096), "gate": (12288, 4096),
-                         "down": (4096, 12288)}.items():
-        run_shape("8b_" + name, N, K, 8, synthetic.LARGE_8BIT, (1, 2, 4, 6, 8, 12, 16, 17), 60 + N + K)
-    run_shape("tiny_4bit_1024", 1024, 1024, 4, synthetic.TINY_4BIT, (1, 2, 4, 8), 70)
+    for name, (N, K, bits, Ms) in PROJ_SHAPES.items():
+        stats = synthetic.LARGE_8BIT if bits == 8 else synthetic.TINY_4BIT
+        run_shape(name, N, K, bits, stats, Ms, 60 + N + K if bits == 8 else 70)
     torch.cuda.empty_cache()
     return {"note": "µs per sv_qmm_verify call (activation preparation + matmul) within a CUDA graph that cycles "
                     "through the weight copies, median; GB/s = weight bytes / time",
@@ -486,6 +493,32 @@ def oracle_sample(shape, M, temperature, seed=7):
     return est * 1e6, time.perf_counter() - spent
 
 
+def oracle_projection_sample(reps=3, seed=11):
+    """The CPU oracle's qmm_verify on SAMPLE_ROWS weight rows of each single
+    projection, at every row count of PROJ_SHAPES, scaled to the projection's
+    N rows: estimated µs per call (median of `reps`)."""
+    import numpy as np
+    from oracle import qmm as oq
+    import synthetic
+    r = synthetic.rng(seed)
+    out = {}
+    for name, (N, K, bits, Ms) in PROJ_SHAPES.items():
+        stats = synthetic.LARGE_8BIT if bits == 8 else synthetic.TINY_4BIT
+        R = min(SAMPLE_ROWS, N)
+        w = synthetic.quant_weight(r, R, K, bits, stats)
+        res = {}
+        for M in Ms:
+            x = synthetic.activations(r, M, K)
+            ts = []
+            for _ in range(reps):
+                t0 = time.perf_counter()
+                oq.qmm_verify(w["wq"], w["scales"], w["biases"], K, bits, x)
+                ts.append((time.perf_counter() - t0) * N / R)
+            res[str(M)] = round(statistics.median(ts) * 1e6, 1)
+        out[name] = res
+    return out
+
+
 SAMPLE_NOTE = ("%d weight rows of each projection of one layer (with the RMSNorm, SwiGLU and residual glue) and of "
                "the vocab head, each scaled by the rows it stands for in the round, plus the accept step on the "
                "full-width rows; extrapolated to one round" % SAMPLE_ROWS)
@@ -494,6 +527,10 @@ SAMPLE_NOTE = ("%d weight rows of each projection of one layer (with the RMSNorm
 def cpu_sample_main(args):
     """--cpu-sample: run the oracle sample `reps` times in this process (the
     caller sets the BLAS thread count in the environment) and print a JSON line."""
+    if args.cpu_proj:
+        oracle_projection_sample(1)                         # warm
+        print(json.dumps(oracle_projection_sample(args.reps)))
+        return
     M = args.only_m or 8
     oracle_sample(SHAPE_8B, M, TEMPERATURE)                 # warm
     runs = [oracle_sample(SHAPE_8B, M, TEMPERATURE) for _ in range(args.reps)]
@@ -517,6 +554,15 @@ def cpu_baseline(M, reps):
             continue
         d = json.loads(r.stdout.strip().splitlines()[-1])
         out[label] = {"value": d["us_median"], "cores": threads, "cpu_seconds": round(d["seconds"], 2)}
+    # single projections of the one-layer sweeps on one core, beside the GPU's `projections`
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-sample", "--cpu-proj", "--reps", "3"],
+                       env=env, capture_output=True, text=True, timeout=900)
+    out["projections_single_core"] = (
+        {"us_per_call": json.loads(r.stdout.strip().splitlines()[-1]), "cores": 1,
+         "sample": "%d weight rows of each projection, scaled to its N rows; median of 3" % SAMPLE_ROWS}
+        if r.returncode == 0 else {"error": r.stderr[-400:]})
     return out
 
 
@@ -536,6 +582,7 @@ def main():
     ap.add_argument("--only-m", type=int, default=0, help="time only this row count (default: 1, 8 and 16)")
     ap.add_argument("--cpu-sample", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--reps", type=int, default=3, help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-proj", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.cpu_sample:
         return cpu_sample_main(args)
@@ -589,7 +636,8 @@ def main():
         allc = cb.get("all_cores", {})
         cpu = {"value": allc.get("value"), "unit": "us/round", "cores": allc.get("cores"), "kind": "oracle",
                "sample": SAMPLE_NOTE, "single_core": cb.get("single_core"), "all_cores": allc,
-               "rule": "the same sample as bench.py --impl reference"}
+               "rule": "the same sample as bench.py --impl reference",
+               "projections_single_core": cb.get("projections_single_core")}
     import __graft_entry__
     __graft_entry__.build()
     from speculative_decoding_verify_qmm_gb300 import binding
