@@ -13,9 +13,10 @@
  *     that need scratch space take a caller-provided workspace whose size comes
  *     from the matching *_workspace_bytes() query, 256-byte aligned.  A
  *     workspace must be zero filled once after allocation (e.g.
- *     cudaMemsetAsync over all of it): it holds a 256 KiB block of counters
- *     and the split-tile partial sums, which every successful call leaves at
- *     zero again, so one workspace (sized for the largest call) can serve any
+ *     cudaMemsetAsync over all of it): it holds a 256 KiB block of counters,
+ *     the split-tile partial sums and (for a round) the gate/up partner
+ *     values, which every successful call leaves at zero again, so one
+ *     workspace (sized for the largest call) can serve any
  *     sequence of calls ordered on one stream.  After a call that reported a
  *     device error, zero it again before reuse.
  *   - bf16 and fp16 values are passed as uint16_t bit patterns.
