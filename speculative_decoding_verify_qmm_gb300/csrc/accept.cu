@@ -179,6 +179,7 @@ __global__ void __launch_bounds__(ACC_THREADS) accept_kernel(const AcceptParams 
   __syncthreads();
   if (!s_last) return;
   __threadfence();
+  if (tid < j) p.out_tokens[r0 + tid] = p.draft[qd0 + tid];  // the accepted drafts (j <= 31), one thread each
 
   // ---- last CTA of the request: locate u[m] * Z among the chunks (warp 0:
   // lane l holds chunks l and l + 32; inclusive scans by shuffles)
@@ -292,7 +293,6 @@ __global__ void __launch_bounds__(ACC_THREADS) accept_kernel(const AcceptParams 
       for (int w = 0; w < ACC_THREADS / 32; ++w) lastp = max(lastp, s_i[ACC_THREADS / 32 + w]);
       token = lastp < 0 ? c1 - 1 : lastp;
     }
-    for (int i = 0; i < j; ++i) p.out_tokens[r0 + i] = p.draft[qd0 + i];
     p.out_tokens[r0 + j] = token;
     p.out_len[b] = j + 1;
   }
