@@ -54,3 +54,24 @@ def test_full_vocab_head_sampled_rows(lib, K, bits, M, T):
     assert_close_rms(lg[:, rows], want, what="sampled logits")
     _check_stats(lg, rmax.cpu().numpy(), rsum.cpu().numpy(), am, T)
     assert lib.device_error() == 0
+
+
+@pytest.mark.parametrize("M,T", [(4, 0.7), (8, 0.0)])
+def test_head_beyond_4096_tiles(lib, M, T):
+    """A vocabulary of more than 4096 64-row tiles (V = 263144): the per-row merge
+    of the tile statistics walks its tiles in several register-held chunks.  Row
+    statistics against the GPU's own logits, logits on sampled rows."""
+    V, K, bits = 4112 * 64 + 40, 512, 4
+    r = synthetic.rng(450 + M)
+    w = synthetic.quant_weight(r, V, K, bits, synthetic.TINY_4BIT)
+    x = synthetic.activations(r, M, K)
+    dw = dev_weight(w)
+    logits, rmax, rsum, rarg = lib.lm_head_verify(dw["wq"], dw["scales"], dw["biases"], K, bits, dev_bf16(x), T)
+    torch.cuda.synchronize()
+    lg = logits.cpu().numpy()
+    am = rarg.cpu().numpy()
+    rows = np.unique(np.concatenate([r.choice(V, 2000, replace=False), am, [0, V - 1, 4096 * 64, 4096 * 64 - 1]]))
+    want = oq.qmm_f32(*[sub_weight(w, rows)[k] for k in ("wq", "scales", "biases")], K, bits, x)
+    assert_close_rms(lg[:, rows], want, what="sampled logits")
+    _check_stats(lg, rmax.cpu().numpy(), rsum.cpu().numpy(), am, T)
+    assert lib.device_error() == 0
