@@ -229,23 +229,47 @@ def kernel_roofline(rnd, reps):
 
 
 def e2e_rounds(rnd, steps):
-    """Host buffers in, host result out: pinned H2D of the round's inputs, the
-    round, D2H of out_len/out_tokens, each step; wall clock per round."""
+    """Host buffers in, host result out, through the public call: each step
+    copies the round's inputs in from pinned host memory (the hidden rows on
+    the round's stream; q, drafts and uniforms on a second stream, which the
+    accept step waits for through accept_wait_event, so that copy overlaps
+    the projections), runs the round, and reads out_len / out_tokens back;
+    wall clock per round.  The copies and the round are one CUDA graph."""
     import torch
     host = [t.cpu().pin_memory() for t in (rnd.h0, rnd.q, rnd.draft, rnd.u)]
     len_host = torch.zeros_like(rnd.out_len, device="cpu").pin_memory()
     tok_host = torch.zeros_like(rnd.out_tokens, device="cpu").pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host)
     d2h = len_host.numel() * 4 + tok_host.numel() * 4
+    main, side = torch.cuda.Stream(), torch.cuda.Stream()
+    ready = torch.cuda.Event()
+
+    def step():
+        with torch.cuda.stream(main):
+            rnd.hidden.copy_(host[0], non_blocking=True)
+        side.wait_stream(main)   # after the hidden rows: one copy engine would otherwise queue them behind q
+        with torch.cuda.stream(side):
+            for dev, h in zip((rnd.q, rnd.draft, rnd.u), host[1:]):
+                dev.copy_(h, non_blocking=True)
+            ready.record(side)
+        with torch.cuda.stream(main):
+            rnd.lib.verify_round(rnd.model, rnd.offs, rnd.hidden, rnd.T, rnd.logits, rnd.out_len, rnd.out_tokens,
+                                 rnd.ws, q=rnd.q, draft=rnd.draft, u=rnd.u, stream=main, accept_wait=ready)
+
+    main.wait_stream(torch.cuda.current_stream())
+    step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=main):
+        step()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for _ in range(steps):
-        for dev, h in zip((rnd.h0, rnd.q, rnd.draft, rnd.u), host):
-            dev.copy_(h, non_blocking=True)
-        rnd.replay()
-        len_host.copy_(rnd.out_len, non_blocking=True)
-        tok_host.copy_(rnd.out_tokens, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
+        with torch.cuda.stream(main):
+            g.replay()
+            len_host.copy_(rnd.out_len, non_blocking=True)
+            tok_host.copy_(rnd.out_tokens, non_blocking=True)
+        main.synchronize()
     return (time.perf_counter() - t0) * 1e6 / steps, h2d, d2h
 
 

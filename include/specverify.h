@@ -311,6 +311,11 @@ int sv_swiglu(const uint16_t* g, int ldg, const uint16_t* u, int ldu, int M, int
  *     `stream` just before and after the launch that runs all the projections,
  *     for timing it (recording them adds a dependency that delays that launch
  *     by the previous launch's drain).
+ *   accept_wait_event: optional cudaEvent_t (NULL to skip): `stream` waits
+ *     for it just before the accept step, the only launch that reads q, draft
+ *     and u, so a caller can copy those in on another stream while the
+ *     projections run (no counterpart on the pages: a pipelining hook).  In a
+ *     stream capture the event must be recorded in the same capture.
  * Workspace: sv_round_workspace_bytes(model, M) bytes (zero-fill rule above). */
 typedef struct {
   const uint32_t* wq;
@@ -364,7 +369,7 @@ int sv_round_plan_init(const sv_model* model, void* plan, size_t plan_bytes);
 int sv_verify_round(const sv_model* model, const void* plan, int B, const int32_t* row_offsets, uint16_t* hidden, int ldh,
                     float temperature, const float* q, int ldq, const int32_t* draft, const float* u, float* logits,
                     int ldl, int32_t* out_len, int32_t* out_tokens, void* workspace, size_t workspace_bytes,
-                    void* stream, void* event_start, void* event_stop);
+                    void* stream, void* event_start, void* event_stop, void* accept_wait_event);
 
 /* ------------------------------------------------------- draft-cap control ---
  * Host-only (no device work, callable without a GPU).  PyPI page, "The

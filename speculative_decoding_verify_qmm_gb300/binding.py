@@ -87,7 +87,7 @@ _SIGNATURES = {
     "sv_round_plan_init": (_c_int, [_c_model_p, _c_void_p, _c_size_t]),
     "sv_verify_round": (_c_int, [_c_model_p, _c_void_p, _c_int, _c_i32_p, _c_void_p, _c_int, _c_float, _c_void_p, _c_int,
                                  _c_void_p, _c_void_p, _c_void_p, _c_int, _c_void_p, _c_void_p, _c_void_p,
-                                 _c_size_t, _c_void_p, _c_void_p, _c_void_p]),
+                                 _c_size_t, _c_void_p, _c_void_p, _c_void_p, _c_void_p]),
     "sv_lm_head_verify": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_int, _c_int, _c_int, _c_int, _c_void_p,
                                    _c_int, _c_int, _c_float, _c_void_p, _c_int, _c_void_p, _c_void_p, _c_void_p,
                                    _c_void_p, _c_size_t, _c_void_p]),
@@ -358,8 +358,10 @@ class Library:
         return self.lib.sv_round_workspace_bytes(ctypes.byref(model), rows)
 
     def verify_round(self, model, row_offsets, hidden, temperature, logits, out_len, out_tokens, workspace,
-                     q=None, draft=None, u=None, stream=None, events=None):
-        """events: optional (start, stop) torch.cuda.Event pair recorded around the matmul launch."""
+                     q=None, draft=None, u=None, stream=None, events=None, accept_wait=None):
+        """events: optional (start, stop) torch.cuda.Event pair recorded around the matmul launch;
+        accept_wait: optional torch.cuda.Event the accept step waits for (q, draft and u copied in
+        on another stream while the projections run)."""
         B = len(row_offsets) - 1
         offs = (ctypes.c_int32 * (B + 1))(*[int(v) for v in row_offsets])
         ev0 = ev1 = None
@@ -369,7 +371,7 @@ class Library:
             ctypes.byref(model), _ptr(model.plan), B, offs, _ptr(hidden), hidden.stride(0), float(temperature), _ptr(q),
             q.stride(0) if q is not None else 0, _ptr(draft), _ptr(u), _ptr(logits), logits.stride(0),
             _ptr(out_len), _ptr(out_tokens), _ptr(workspace), workspace.numel() * workspace.element_size(),
-            _stream(stream), ev0, ev1))
+            _stream(stream), ev0, ev1, ctypes.c_void_p(accept_wait.cuda_event) if accept_wait is not None else None))
 
     # --------------------------------------------------------------- accept
     def accept_workspace_bytes(self, B, rows):

@@ -169,7 +169,7 @@ int sv_round_plan_init(const sv_model* model, void* plan, size_t plan_bytes) {
 int sv_verify_round(const sv_model* model, const void* plan, int B, const int32_t* row_offsets, uint16_t* hidden, int ldh,
                     float temperature, const float* q, int ldq, const int32_t* draft, const float* u, float* logits,
                     int ldl, int32_t* out_len, int32_t* out_tokens, void* workspace, size_t workspace_bytes,
-                    void* stream, void* event_start, void* event_stop) {
+                    void* stream, void* event_start, void* event_stop, void* accept_wait_event) {
   if (B < 1 || !row_offsets) return fail(SV_EINVAL, "B must be >= 1 with row offsets");
   const int M = row_offsets[B];
   if (M < 1 || M > MAX_M) return fail(M > MAX_M ? SV_EUNSUPPORTED : SV_EINVAL, "total rows %d not in [1, 32]", M);
@@ -246,6 +246,8 @@ int sv_verify_round(const sv_model* model, const void* plan, int B, const int32_
     return cuda_fail(e, "record event_stop");
   e = launch_lmhead_finalize(p.tile_stats, (model->vocab + BN - 1) / BN, p.MP, M, p.inv_temp, rmax, rsum, rarg, s);
   if (e != cudaSuccess) return cuda_fail(e, "lm_head finalize launch");
+  if (accept_wait_event && (e = cudaStreamWaitEvent(s, static_cast<cudaEvent_t>(accept_wait_event), 0)) != cudaSuccess)
+    return cuda_fail(e, "wait for accept_wait_event");
   return accept_internal(B, row_offsets, logits, ldl, rmax, temperature > 0.f ? rsum : nullptr, rarg, q, ldq, draft,
                          model->vocab, temperature, u, out_len, out_tokens, workspace, s);
 }

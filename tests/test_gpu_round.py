@@ -119,6 +119,63 @@ def test_batched_round_four_requests(lib):
         assert (int(n[b]), toks[offs[b]:offs[b] + n[b]].tolist()) == tuple(want[b])
 
 
+def test_round_accept_inputs_on_a_side_stream(lib):
+    """q, draft and u copied in from pinned host memory on another stream while the
+    projections run, the accept step waiting for them (accept_wait_event), inside a
+    captured CUDA graph: the same bits as the round with its inputs resident."""
+    layers, head = _model.host_model(1500, 2, bits=8, stats=synthetic.LARGE_8BIT, **TINY)
+    model = lib.make_model(_model.device_layers(layers), _model.to_device(head), TINY["hidden"], TINY["q_dim"],
+                           TINY["inter"], TINY["vocab"], 8)
+    r = synthetic.rng(1501)
+    m = 7
+    M = m + 1
+    h0 = synthetic.activations(r, M, TINY["hidden"])
+    qn = synthetic.logits_and_draft_probs(r, m, TINY["vocab"])[1]
+    dn = synthetic.sample_drafts(r, qn)
+    un = synthetic.accept_uniforms(r, M)
+    # reference: everything resident before the call
+    ref = _round(lib, model, [0, M], dev_bf16(h0), 1.0, q=torch.from_numpy(qn).cuda(),
+                 draft=torch.from_numpy(dn).cuda(), u=torch.from_numpy(un).cuda())
+    # the pipelined form, captured once and replayed
+    hq, hd, hu = (torch.from_numpy(a).pin_memory() for a in (qn, dn, un))
+    q, d, u = (torch.empty_like(a, device="cuda") for a in (hq, hd, hu))
+    hidden = dev_bf16(h0)
+    h_init = hidden.clone()
+    logits = torch.zeros((M, TINY["vocab"]), dtype=torch.float32, device="cuda")
+    out_len = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out_tokens = torch.full((M,), -1, dtype=torch.int32, device="cuda")
+    ws = lib.workspace(lib.round_workspace_bytes(model, M))
+    ready = torch.cuda.Event()
+    main, side = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def step():
+        side.wait_stream(main)
+        with torch.cuda.stream(side):
+            for dev, host in ((q, hq), (d, hd), (u, hu)):
+                dev.copy_(host, non_blocking=True)
+            ready.record(side)
+        with torch.cuda.stream(main):
+            hidden.copy_(h_init)
+            lib.verify_round(model, [0, M], hidden, 1.0, logits, out_len, out_tokens, ws, q=q, draft=d, u=u,
+                             stream=main, accept_wait=ready)
+
+    main.wait_stream(torch.cuda.current_stream())
+    step()                                   # eager once (kernel attributes are set outside capture)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=main):
+        step()
+    for _ in range(2):
+        q.zero_()
+        d.zero_()
+        u.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(hidden, ref[0]) and torch.equal(logits, ref[1])
+        assert (out_len.cpu().numpy() == ref[2]).all() and (out_tokens.cpu().numpy() == ref[3]).all()
+    assert lib.device_error() == 0
+
+
 def _unpack_host(packed, N, K, bits):
     """Canonical (codes bytes [N, K*bits/8], scales, biases) read back from a unit-packed buffer,
     following the layout sv_qmm_pack documents: per (tile, chunk) unit, 128-byte pieces x 64 rows
