@@ -455,11 +455,36 @@ def wide(lib, steps, warmup, peaks):
         out[name] = {"N": N, "K": K, "M": M, "us": round(t, 2), "tflops": round(tf, 1),
                      "weight_gbs": round(per / (t * 1e-6) / 1e9, 1), "copies_rotated": copies}
         del ws
+    # the gate|up shape across block widths: the tensor-memory kernel from 33 rows up, the
+    # weight-streaming kernel at 32 for comparison
+    N, K, bits = 24576, 4096, 8
+    per = N * K * (bits / 8 + 4 / 64)
+    copies = max(2, int(np.ceil(2 * L2_BYTES / per)) + 1)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(N + K + 1)
+    ws = [synthetic.device_quant_weight(gen, N, K, bits, synthetic.LARGE_8BIT) for _ in range(copies)]
+    by_m = {}
+    for M in (32, 33, 64, 128, 256, 512):
+        x = torch.randn((M, K), device="cuda", dtype=torch.bfloat16)
+        y = torch.empty((M, N), device="cuda", dtype=torch.bfloat16)
+        wsp = lib.workspace(lib.qmm_workspace_bytes(M, N, K, bits))
+
+        def calls_m():
+            for w in ws:
+                lib.qmm_verify(w["wq"], w["scales"], w["biases"], K, bits, x, y=y, workspace=wsp)
+        g = graph_of(calls_m)
+        t = statistics.median(time_replays(g.replay, max(10, steps // 2), warmup)) / copies
+        by_m[str(M)] = {"us": round(t, 2), "tflops": round(2.0 * M * N * K / (t * 1e-6) / 1e12, 1),
+                        "weight_gbs": round(per / (t * 1e-6) / 1e9, 1)}
+    del ws
     top = out["gate_up"]
     torch.cuda.empty_cache()
     return {"workload": "8-bit g64 projections at M = 512 rows through sv_qmm_verify (tcgen05.mma, fp16 operands, "
                         "fp32 accumulators in tensor memory)",
             "by_shape": out,
+            "gate_up_by_M": by_m,
+            "gate_up_by_M_note": "sv_qmm_verify on the 24576 x 4096 gate|up shape per block width; M = 32 runs the "
+                                 "weight-streaming kernel, M >= 33 the tensor-memory kernel",
             "roofline": {"bound": "tensor", "achieved": top["tflops"], "peak": tf_peak, "unit": "TFLOP/s",
                          "frac": round(top["tflops"] / tf_peak, 3), "traffic": None,
                          "kernel": "wide_kernel<8> (gate_up 24576 x 4096, M = 512), whole call incl. preparation "
