@@ -298,38 +298,56 @@ static WidePlan wide_plan(int M, int N, int K, int bits, int sms) {
   w.chunk = w.Mpad / w.mchunks;
   const int codes = WT * WK * bits / 8;
   w.stage_bytes = (wide_codes_off(w.chunk) + codes + 2 * WT * 16 + 1023) / 1024 * 1024;
-  const int budget = 226 * 1024 - 1024;  // 1 KB of it aligns the stages
-  w.stages = budget / w.stage_bytes;
-  if (w.stages > W_MAX_STAGES) w.stages = W_MAX_STAGES;
-  w.smem = 1024 + w.stages * w.stage_bytes;
   w.tiles = (N + WT - 1) / WT;
   w.ks_total = K / WK;
-  // k splits, in units of the whole GPU's compute time for the projection:
-  // waves of CTAs (sms / items * ceil(items * s / sms) / s, items = tiles x
-  // row chunks) plus, for s > 1,
-  // the HBM time of writing and re-reading the fp32 partials, which relative
-  // to the compute time is about 0.27 * s * 4096 / K (8 B per output per
-  // split against 2 K flops per output at this part's bf16 rate and copy
-  // bandwidth); at least 8 k-steps per split
-  int splits = 1;
+  uint32_t cols = 32;  // tensor-memory columns of one CTA's accumulators
+  while ((int)cols < w.chunk) cols <<= 1;
+  // Each k-step of a CTA is a chain of a copy, barrier hops, the dequantizing
+  // and the MMAs, so a CTA's time is about (k-steps) x (a + b / stages): with
+  // the arithmetic left out, 0.51 / 0.64 / 0.77 us per step at 6 / 3 / 2
+  // stages (a = 0.4, b = 0.8).  A grid past the SM count runs in waves, so
+  // two CTAs per SM (half the stages each, when their tensor memory and
+  // shared memory fit) can beat one CTA with a deep ring: the 192 gate|up
+  // tiles at 64 rows take 103 us in two waves of one CTA per SM and 72 us in
+  // one wave of two.  k splits cut the k-steps per CTA at the cost of
+  // writing and re-reading fp32 partials: about 0.27 * s * 4096 / K of the
+  // projection's compute time (8 B per output per split against 2 K flops per
+  // output at this part's bf16 rate and copy bandwidth); at least 8 k-steps
+  // per split.
+  const int items = w.tiles * w.mchunks;
+  const int max_split = w.ks_total / 8 > 0 ? w.ks_total / 8 : 1;
+  const int one_sm_budget = 226 * 1024 - 1024;  // one CTA per SM; 1 KB of it aligns the stages
+  const int two_sm_budget = 228 * 1024 / 2 - 2048 - 1024;  // per CTA: system reserve and barriers, alignment
+  int best_stages = one_sm_budget / w.stage_bytes, best_split = 1;
+  if (best_stages > W_MAX_STAGES) best_stages = W_MAX_STAGES;
   if (sms > 0) {
-    const int max_split = w.ks_total / 8 > 0 ? w.ks_total / 8 : 1;
     double best = 1e30;
-    for (int sp = 1; sp <= max_split && sp <= 16; ++sp) {
-      const int items = w.tiles * w.mchunks;
-      const double waves = (double)sms / items * (double)((items * sp + sms - 1) / sms) / sp;
-      const double cost = waves + (sp > 1 ? 0.27 * sp * 4096.0 / K : 0.0);
-      if (cost < best - 1e-12) {
-        best = cost;
-        splits = sp;
+    for (int per_sm = 1; per_sm <= 2; ++per_sm) {
+      int st = (per_sm == 1 ? one_sm_budget : two_sm_budget) / w.stage_bytes;
+      if (st > W_MAX_STAGES) st = W_MAX_STAGES;
+      if (st < 2 || per_sm * cols > 512) continue;
+      const long long slots = (long long)sms * per_sm;
+      const double step = 0.4 + 0.8 / st;
+      for (int sp = 1; sp <= max_split && sp <= 16; ++sp) {
+        const double waves = (double)((items * (long long)sp + slots - 1) / slots);
+        const double ksteps = (double)((w.ks_total + sp - 1) / sp);
+        const double partials = sp > 1 ? 0.27 * sp * 4096.0 / K * ((double)items * w.ks_total / sms) : 0.0;
+        const double cost = step * (waves * ksteps + partials);
+        if (cost < best * (1.0 - 1e-9)) {
+          best = cost;
+          best_stages = st;
+          best_split = sp;
+        }
       }
     }
   }
-  w.splits = splits;
+  w.stages = best_stages;
+  w.splits = best_split;
+  w.smem = 1024 + w.stages * w.stage_bytes;
   size_t off = COUNTER_BYTES;
   w.x16 = off;      off = align256(off + (size_t)w.Mpad * K * 2);
   w.inv = off;      off = align256(off + (size_t)w.Mpad * 4);
-  w.partials = off; off = align256(off + (splits > 1 ? (size_t)splits * M * N * 4 : 0));
+  w.partials = off; off = align256(off + (w.splits > 1 ? (size_t)w.splits * M * N * 4 : 0));
   w.total = off;
   return w;
 }
