@@ -302,18 +302,21 @@ static WidePlan wide_plan(int M, int N, int K, int bits, int sms) {
   w.ks_total = K / WK;
   uint32_t cols = 32;  // tensor-memory columns of one CTA's accumulators
   while ((int)cols < w.chunk) cols <<= 1;
-  // Each k-step of a CTA is a chain of a copy, barrier hops, the dequantizing
-  // and the MMAs, so a CTA's time is about (k-steps) x (a + b / stages): with
-  // the arithmetic left out, 0.51 / 0.64 / 0.77 us per step at 6 / 3 / 2
-  // stages (a = 0.4, b = 0.8).  A grid past the SM count runs in waves, so
-  // two CTAs per SM (half the stages each, when their tensor memory and
-  // shared memory fit) can beat one CTA with a deep ring: the 192 gate|up
-  // tiles at 64 rows take 103 us in two waves of one CTA per SM and 72 us in
-  // one wave of two.  k splits cut the k-steps per CTA at the cost of
-  // writing and re-reading fp32 partials: about 0.27 * s * 4096 / K of the
-  // projection's compute time (8 B per output per split against 2 K flops per
-  // output at this part's bf16 rate and copy bandwidth); at least 8 k-steps
-  // per split.
+  // Time model of a plan (CTAs per SM, stages S, k splits s), in us: each
+  // k-step of a CTA is a chain of a copy, barrier hops, the dequantizing and
+  // the MMAs, and each wave of CTAs has a fixed part (pipeline fill,
+  // tensor-memory set-up, epilogue):
+  //   waves x (k-steps x (0.57 + 0.72 / S + per_sm x (0.0005 rows - 0.009))
+  //            + 3.3 + 0.017 rows)
+  //   + for s > 1: 2.3e-6 x M x N x s (fp32 partials out and back) + 5.3.
+  // Least-squares fit to 256 forced plans (one or two CTAs per SM, 1-16
+  // splits; 8-bit gate|up, down and q and 4-bit gate|up and down shapes at 33,
+  // 64, 128, 256 and 512 rows): median error 5 %, and the plan it picks is
+  // the measured best or within 6 % of it for every shape and width.  Two
+  // CTAs per SM (half the stages each, when their tensor memory and shared
+  // memory fit) win when they put the grid in fewer waves, e.g. the 192
+  // gate|up tiles at 64 rows: 103 us in two waves of one CTA per SM, 72 in one
+  // wave of two.
   const int items = w.tiles * w.mchunks;
   const int max_split = w.ks_total / 8 > 0 ? w.ks_total / 8 : 1;
   const int one_sm_budget = 226 * 1024 - 1024;  // one CTA per SM; 1 KB of it aligns the stages
@@ -327,12 +330,13 @@ static WidePlan wide_plan(int M, int N, int K, int bits, int sms) {
       if (st > W_MAX_STAGES) st = W_MAX_STAGES;
       if (st < 2 || per_sm * cols > 512) continue;
       const long long slots = (long long)sms * per_sm;
-      const double step = 0.4 + 0.8 / st;
+      const double step_us = 0.57 + 0.72 / st + per_sm * (0.0005 * w.chunk - 0.009);
+      const double wave_us = 3.3 + 0.017 * w.chunk;
       for (int sp = 1; sp <= max_split && sp <= 16; ++sp) {
         const double waves = (double)((items * (long long)sp + slots - 1) / slots);
         const double ksteps = (double)((w.ks_total + sp - 1) / sp);
-        const double partials = sp > 1 ? 0.27 * sp * 4096.0 / K * ((double)items * w.ks_total / sms) : 0.0;
-        const double cost = step * (waves * ksteps + partials);
+        const double partials_us = sp > 1 ? 2.3e-6 * M * (double)N * sp + 5.3 : 0.0;
+        const double cost = waves * (ksteps * step_us + wave_us) + partials_us;
         if (cost < best * (1.0 - 1e-9)) {
           best = cost;
           best_stages = st;
