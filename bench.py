@@ -494,6 +494,118 @@ def wide(lib, steps, warmup, peaks):
             "hbm_peak_gbs": hbm}
 
 
+def bits2_round(lib, steps, warmup, hbm):
+    """The 27B-class round with 2-bit codes (the pages' 2-bit target, whose
+    verify rows turn compute-bound early) at M = 1..8: us per round and the
+    cost ratio against M = 1."""
+    import torch
+    import synthetic
+    shape = dict(SHAPE_27B, bits=2)
+    layers, head = device_model(lib, 2222, shape, synthetic.TINY_2BIT)
+    wb = weight_bytes(shape)
+    curve = {}
+    for M in (1, 2, 3, 4, 6, 8):
+        rnd = Round(lib, layers, head, shape, M, 1, seed=900 + M, temperature=TEMPERATURE)
+        rnd.capture()
+        curve[M] = statistics.median(time_replays(rnd.replay, steps, warmup))
+        del rnd
+    del layers, head
+    torch.cuda.empty_cache()
+    t1 = curve[1]
+    return {"workload": "27B-class verify round with 2-bit g64 codes: 64 layers, hidden 5120, q 6144, kv 1024, "
+                        "inter 17408, lm_head 5120->151936, T = 0.7, unit-packed weights",
+            "weight_bytes_per_round": wb,
+            "us_per_round": {str(k): round(v, 2) for k, v in curve.items()},
+            "cost_ratio_vs_M1": {str(k): round(v / t1, 3) for k, v in curve.items()},
+            "weight_stream_gbs": {str(k): round(wb / (v * 1e-6) / 1e9, 1) for k, v in curve.items()},
+            "roofline": {"bound": "hbm", "achieved": round(wb / (t1 * 1e-6) / 1e9, 1), "peak": hbm, "unit": "GB/s",
+                         "frac": round(wb / (t1 * 1e-6) / 1e9 / hbm, 3), "traffic": None,
+                         "note": "whole round at M = 1 (weight bytes / replay time)"}}
+
+
+def moe_gather(lib, steps, warmup, hbm):
+    """Mixture-of-experts verify rows through sv_gather_qmm: 128 experts, each
+    row routed to 8 of them (a 30B-A3B-class expert layer, gate|up 2 x 768 x
+    2048, 4-bit).  Every extra verify row pulls in more experts: us per call
+    and the distinct experts' bytes per call, over 16 route sets per width."""
+    import numpy as np
+    import torch
+    import synthetic
+    E, N, K, bits, top = 128, 2 * 768, 2048, 4, 8
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(3030)
+    w = synthetic.device_quant_weight(gen, E * N, K, bits, synthetic.TINY_4BIT)
+    per_expert = N * K * (bits / 8 + 4 / 64)
+    r = synthetic.rng(3031)
+    out = {}
+    for M in (1, 2, 4, 8, 16):
+        x = synthetic.device_activations(gen, M, K)
+        sets, distinct = [], []
+        for _ in range(16):
+            rows = np.repeat(np.arange(M, dtype=np.int32), top)
+            exps = np.concatenate([r.choice(E, top, replace=False) for _ in range(M)]).astype(np.int32)
+            sets.append((torch.from_numpy(rows).cuda(), torch.from_numpy(exps).cuda()))
+            distinct.append(len(set(exps.tolist())))
+        P = M * top
+        y = torch.empty((P, N), dtype=torch.bfloat16, device="cuda")
+        wsp = lib.workspace(lib.lib.sv_gather_qmm_workspace_bytes(P, M, N, K, E, bits))
+
+        def calls():
+            for pr, pe in sets:
+                lib.gather_qmm(w["wq"], w["scales"], w["biases"], E, K, bits, x, pr, pe, y=y, workspace=wsp)
+        g = graph_of(calls)
+        t = statistics.median(time_replays(g.replay, max(10, steps // 2), warmup)) / len(sets)
+        eb = statistics.fmean(distinct) * per_expert
+        out[str(M)] = {"us": round(t, 2), "distinct_experts": round(statistics.fmean(distinct), 1),
+                       "expert_bytes": round(eb), "gbs": round(eb / (t * 1e-6) / 1e9, 1)}
+    del w
+    torch.cuda.empty_cache()
+    top_m = out["16"]
+    return {"workload": "gather-qmm over 128 stacked 4-bit g64 experts (gate|up 1536 x 2048 each), 8 experts per "
+                        "row, M = 1..16 verify rows; 16 random route sets per width in one CUDA graph",
+            "by_M": out,
+            "roofline": {"bound": "hbm", "achieved": top_m["gbs"], "peak": hbm, "unit": "GB/s",
+                         "frac": round(top_m["gbs"] / hbm, 3), "traffic": None,
+                         "note": "M = 16: distinct selected experts' bytes / call time"}}
+
+
+def accept_variants(lib, steps, warmup, hbm):
+    """The accept step's f2 variants at the full vocabulary (V = 151936, m = 7,
+    T = 0.8): lossless top-k / top-p truncated accept, the truncated draft
+    probabilities, and log-probabilities with the top 5 from the logits."""
+    import numpy as np
+    import torch
+    import synthetic
+    r = synthetic.rng(4040)
+    V, m, T = 151936, 7, 0.8
+    z, q = synthetic.logits_and_draft_probs(r, m, V)
+    draft = synthetic.sample_drafts(r, q)
+    u = synthetic.accept_uniforms(r, m + 1)
+    dz, dq = torch.from_numpy(z).cuda(), torch.from_numpy(q).cuda()
+    dd, du = torch.from_numpy(draft).cuda(), torch.from_numpy(u).cuda()
+    chosen = torch.from_numpy(np.argmax(z, axis=1).astype(np.int32)).cuda()
+    ws = lib.workspace(lib.accept_workspace_bytes(1, m + 1))
+    probs_out = torch.empty_like(dq)
+    cases = {
+        "accept_plain": (lambda: lib.spec_accept_truncated([0, m + 1], dz, dd, T, 0, 1.0, q=dq, u=du, workspace=ws),
+                         (2 * m + 1) * V * 4),
+        "accept_top_k_50_top_p_0.9": (lambda: lib.spec_accept_truncated([0, m + 1], dz, dd, T, 50, 0.9, q=dq, u=du,
+                                                                          workspace=ws), (2 * m + 1) * V * 4),
+        "truncate_probs_top_p_0.9": (lambda: lib.truncate_probs(dq, 0, 0.9, out=probs_out), 2 * m * V * 4),
+        "logprobs_top5": (lambda: lib.logprobs(dz, T, chosen=chosen, top_n=5), (m + 1) * V * 4),
+    }
+    out = {}
+    for name, (fn, nbytes) in cases.items():
+        g = graph_of(fn)
+        t = statistics.median(time_replays(g.replay, max(20, steps), warmup))
+        out[name] = {"us": round(t, 2), "bytes_read": nbytes, "gbs": round(nbytes / (t * 1e-6) / 1e9, 1)}
+    if lib.device_error():
+        raise SystemExit("device error in the accept variants")
+    return {"workload": "V = 151936, m = 7 drafts, T = 0.8, one request; each call replayed from a CUDA graph",
+            "calls": out,
+            "note": "latency-bound: a few passes over 8 rows of 608 KB from L2"}
+
+
 # ---------------------------------------------------------- CPU oracle leg
 SAMPLE_ROWS = 256
 
@@ -738,6 +850,9 @@ def main():
         extra["batched_27b"] = batched_27b(lib, args.steps, args.warmup, hbm)
         extra["projections"] = projections(lib, args.steps, args.warmup, hbm)
         extra["wide"] = wide(lib, args.steps, args.warmup, peaks)
+        extra["bits2_27b"] = bits2_round(lib, args.steps, args.warmup, hbm)
+        extra["moe_gather"] = moe_gather(lib, args.steps, args.warmup, hbm)
+        extra["accept_variants"] = accept_variants(lib, args.steps, args.warmup, hbm)
         if lib.device_error():
             raise SystemExit("device error after the additional workloads")
 

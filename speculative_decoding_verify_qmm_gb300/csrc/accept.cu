@@ -309,7 +309,7 @@ __global__ void __launch_bounds__(1024) row_stats_kernel(const float* __restrict
   const float* z = logits + (size_t)r * ldl;
   __shared__ float sb[1024];
   __shared__ int si[1024];
-  __shared__ double sd[1024];
+  __shared__ u128 sd[32];
   float best = -INFINITY;
   int bi = 0x7fffffff;
   for (int k = tid; k < V; k += 1024) {
@@ -329,20 +329,23 @@ __global__ void __launch_bounds__(1024) row_stats_kernel(const float* __restrict
   }
   best = sb[0];
   bi = si[0];
-  if (temperature > 0.f) {
-    double acc = 0.0;
-    for (int k = tid; k < V; k += 1024) acc += (double)exp_term((z[k] - best) / temperature);
-    sd[tid] = acc;
+  double se = 0.0;
+  if (temperature > 0.f) {  // the fp32 exp terms summed exactly (fixed point)
+    u128 acc = 0;
+    for (int k = tid; k < V; k += 1024) acc += to_fixed(exp_term((z[k] - best) / temperature));
+    acc = warp_sum_u128(acc);
+    if ((tid & 31) == 0) sd[tid >> 5] = acc;
     __syncthreads();
-    for (int w = 512; w; w >>= 1) {
-      if (tid < w) sd[tid] += sd[tid + w];
-      __syncthreads();
+    if (tid == 0) {
+      u128 t = 0;
+      for (int w = 0; w < 32; ++w) t += sd[w];
+      se = fixed_to_double(t);
     }
   }
   if (tid == 0) {
     row_max[r] = best;
     row_argmax[r] = bi;
-    if (temperature > 0.f) row_sumexp[r] = (float)sd[0];
+    if (temperature > 0.f) row_sumexp[r] = (float)se;
   }
 }
 

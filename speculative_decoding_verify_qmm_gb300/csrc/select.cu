@@ -16,6 +16,15 @@
 // the key's four bytes (most significant first) finds K - by counts for
 // top_k, by mass for top_p - and one scan over the tied keys finds I.
 // Everything stays in the CTA, so these calls need no workspace.
+//
+// Masses are summed exactly: every weight (a probability, or an fp32 exp
+// term, both at most 1 for valid rows) is a 64.64 fixed-point integer, exact
+// for weights from 2^-40 up and truncated below, and integer sums do not
+// depend on their order.  Each warp keeps private 256-bin histograms,
+// updated with shared-memory atomics (a mass as a 64-bit add on its fraction
+// word that carries into its integer word), so a hot bin is contended only
+// within a warp (a probability row puts nearly every key in a handful of
+// top-byte bins).
 #include <cmath>
 
 #include "sv_internal.h"
@@ -34,11 +43,85 @@ struct SelShared {
   int wint[SEL_WARPS];
   int bin;
   double above;
+  double total;
   int ifound;
   int n_top;
   uint32_t top_key[32];
   int top_idx[32];
 };
+
+// Per-warp histograms (dynamic shared memory): counts, and masses as 64.64
+// fixed point split into the fraction word and the integer word.
+struct SelHist {
+  unsigned int cnt[SEL_WARPS][256];
+  unsigned long long lo[SEL_WARPS][256];
+  unsigned long long hi[SEL_WARPS][256];
+  u128 part[SEL_WARPS];
+};
+
+// Exact block-wide sum of per-thread fixed-point values, as a double.
+__device__ double block_sum_fixed(u128 v, SelHist& h, SelShared& sh) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  v = warp_sum_u128(v);
+  __syncthreads();
+  if (lane == 0) h.part[wid] = v;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    u128 t = 0;
+    for (int w = 0; w < SEL_WARPS; ++w) t += h.part[w];
+    sh.total = fixed_to_double(t);
+  }
+  __syncthreads();
+  const double r = sh.total;
+  __syncthreads();
+  return r;
+}
+
+// One radix pass over a row: among the elements whose key matches `prefix`
+// under `pmask` and that `keep` admits, the count (and with WITH_MASS the
+// exact weight sum) per value of the key's byte at `shift`, into sh.cnt /
+// sh.mass; with WITH_MASS, sh.total is the mass of all of them.  Every thread
+// of the block calls it.
+template <bool WITH_MASS, typename Keep, typename Weight>
+__device__ void radix_pass(const float* x, int V, int shift, uint32_t prefix, uint32_t pmask, Keep keep, Weight weight,
+                           SelHist& h, SelShared& sh) {
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  for (int b = lane; b < 256; b += 32) {
+    h.cnt[wid][b] = 0u;
+    if (WITH_MASS) h.lo[wid][b] = h.hi[wid][b] = 0ull;
+  }
+  __syncwarp();
+  for (int v = tid; v < V; v += SEL_THREADS) {
+    const float xv = x[v];
+    const uint32_t key = order_key(xv);
+    if ((key & pmask) != prefix || !keep(key, v)) continue;
+    const int b = (key >> shift) & 255;
+    atomicAdd(&h.cnt[wid][b], 1u);
+    if (WITH_MASS) {
+      const u128 wf = to_fixed(weight(xv));
+      const unsigned long long lo = (unsigned long long)wf, hi = (unsigned long long)(wf >> 64);
+      const unsigned long long old = atomicAdd(&h.lo[wid][b], lo);
+      const unsigned long long carry = old > ~lo ? 1ull : 0ull;  // this add wrapped the fraction word
+      if (hi | carry) atomicAdd(&h.hi[wid][b], hi + carry);
+    }
+  }
+  __syncthreads();
+  u128 m = 0;
+  for (int b = tid; b < 256; b += SEL_THREADS) {
+    unsigned int c = 0u;
+    for (int w = 0; w < SEL_WARPS; ++w) {
+      c += h.cnt[w][b];
+      if (WITH_MASS) m += ((u128)h.hi[w][b] << 64) + h.lo[w][b];
+    }
+    sh.cnt[b] = (int)c;
+    if (WITH_MASS) sh.mass[b] = fixed_to_double(m);
+  }
+  if (WITH_MASS) {
+    block_sum_fixed(m, h, sh);  // sh.total: the exact mass of every admitted element
+  } else {
+    __syncthreads();
+  }
+}
 
 // Sum over the lanes above this one (fixed shuffle order).
 template <typename T>
@@ -153,6 +236,8 @@ __global__ void __launch_bounds__(SEL_THREADS) select_kernel(const SelectArgs p)
   pdl_trigger();
   pdl_wait();
   __shared__ SelShared sh;
+  extern __shared__ __align__(16) uint8_t sel_dyn[];
+  SelHist& h = *reinterpret_cast<SelHist*>(sel_dyn);
   const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
   const float* x = p.x + (size_t)row * p.ldx;
   const int V = p.V;
@@ -169,7 +254,8 @@ __global__ void __launch_bounds__(SEL_THREADS) select_kernel(const SelectArgs p)
     }
   }
   // a token's weight: exp((z - max) / T) exactly as the accept step computes it, or the probability
-  auto weight = [&](float xv) -> double { return probs ? (double)xv : (double)exp_term((xv - xmax) / T); };
+  auto weight = [&](float xv) -> float { return probs ? xv : exp_term((xv - xmax) / T); };
+  auto all = [](uint32_t, int) { return true; };
 
   // ---- top-k: the k-th key in the order (by counts), then its tie index
   const int k_lim = p.mode == SEL_TOPN ? min(p.top_n, V) : p.top_k;
@@ -179,13 +265,7 @@ __global__ void __launch_bounds__(SEL_THREADS) select_kernel(const SelectArgs p)
     uint32_t prefix = 0u, pmask = 0u;
     int need = k_lim;
     for (int shift = 24; shift >= 0; shift -= 8) {
-      for (int b = tid; b < 256; b += SEL_THREADS) sh.cnt[b] = 0;
-      __syncthreads();
-      for (int v = tid; v < V; v += SEL_THREADS) {
-        const uint32_t key = order_key(x[v]);
-        if ((key & pmask) == prefix) atomicAdd(&sh.cnt[(key >> shift) & 255], 1);
-      }
-      __syncthreads();
+      radix_pass<false>(x, V, shift, prefix, pmask, all, weight, h, sh);
       if (tid < 32) find_bin<int>(sh.cnt, need, lane, sh);
       __syncthreads();
       prefix |= (uint32_t)sh.bin << shift;
@@ -204,32 +284,12 @@ __global__ void __launch_bounds__(SEL_THREADS) select_kernel(const SelectArgs p)
   int I = Ik;
   double kept_mass;
   if (p.mode != SEL_TOPN && p.top_p < 1.f) {
-    double w = 0.0;
-    for (int v = tid; v < V; v += SEL_THREADS) {
-      const float xv = x[v];
-      if (kept_k(order_key(xv), v)) w += weight(xv);
-    }
-    const double W = block_sum(w, sh);
-    const double theta = (double)p.top_p * W;
     uint32_t prefix = 0u, pmask = 0u;
-    double above_total = 0.0;
+    double above_total = 0.0, theta = 0.0;
     int ties = 0;
     for (int shift = 24; shift >= 0; shift -= 8) {
-      for (int b = tid; b < 256; b += SEL_THREADS) {
-        sh.cnt[b] = 0;
-        sh.mass[b] = 0.0;
-      }
-      __syncthreads();
-      for (int v = tid; v < V; v += SEL_THREADS) {
-        const float xv = x[v];
-        const uint32_t key = order_key(xv);
-        if ((key & pmask) == prefix && kept_k(key, v)) {
-          const int b = (key >> shift) & 255;
-          atomicAdd(&sh.mass[b], weight(xv));
-          atomicAdd(&sh.cnt[b], 1);
-        }
-      }
-      __syncthreads();
+      radix_pass<true>(x, V, shift, prefix, pmask, kept_k, weight, h, sh);
+      if (shift == 24) theta = (double)p.top_p * sh.total;  // the first pass sees every survivor
       // at least the smallest positive weight: rounding never turns the search upside down
       if (tid < 32) find_bin<double>(sh.mass, fmax(theta - above_total, 4.9e-324), lane, sh);
       __syncthreads();
@@ -246,18 +306,18 @@ __global__ void __launch_bounds__(SEL_THREADS) select_kernel(const SelectArgs p)
       const uint32_t u = (K & 0x80000000u) ? (K & 0x7fffffffu) : ~K;
       xk = __uint_as_float(u);
     }
-    const double wt = weight(xk);
+    const double wt = fixed_to_double(to_fixed(weight(xk)));
     int r = wt > 0.0 ? (int)ceil((theta - above_total) / wt) : ties;
     r = max(1, min(r, ties));
     I = tie_index(x, V, K, K == Kk ? Ik : V - 1, r, sh);
     kept_mass = above_total + (double)r * wt;
   } else if (p.mode != SEL_TOPN) {
-    double w = 0.0;
+    u128 w = 0;
     for (int v = tid; v < V; v += SEL_THREADS) {
       const float xv = x[v];
-      if (kept_k(order_key(xv), v)) w += weight(xv);
+      if (kept_k(order_key(xv), v)) w += to_fixed(weight(xv));
     }
-    kept_mass = block_sum(w, sh);
+    kept_mass = block_sum_fixed(w, h, sh);
   } else {
     kept_mass = 0.0;
   }
@@ -282,9 +342,9 @@ __global__ void __launch_bounds__(SEL_THREADS) select_kernel(const SelectArgs p)
   }
 
   // ---- SEL_TOPN: log-probabilities of the chosen token and of the top_n tokens
-  double s = 0.0;
-  for (int v = tid; v < V; v += SEL_THREADS) s += exp(((double)x[v] - (double)xmax) / (double)T);
-  const double log_s = log(block_sum(s, sh));
+  u128 s = 0;
+  for (int v = tid; v < V; v += SEL_THREADS) s += to_fixed(exp_term((x[v] - xmax) / T));
+  const double log_s = log(block_sum_fixed(s, h, sh));
   if (p.top_n == 0) {
     if (tid == 0 && p.chosen) {
       const int c = p.chosen[row];
@@ -328,8 +388,15 @@ __global__ void __launch_bounds__(SEL_THREADS) select_kernel(const SelectArgs p)
 }
 
 cudaError_t launch_select(const SelectArgs& a, int rows, cudaStream_t s) {
+  static bool attr_set = false;  // the attribute is per function
+  if (!attr_set) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(SelHist));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = pdl_config(dim3(rows), dim3(SEL_THREADS), 0, s, attr);
+  cudaLaunchConfig_t cfg = pdl_config(dim3(rows), dim3(SEL_THREADS), sizeof(SelHist), s, attr);
   return cudaLaunchKernelEx(&cfg, select_kernel, a);
 }
 

@@ -7,6 +7,35 @@ namespace sv {
 
 constexpr int MAX_BATCH = 256;
 
+// Exact sums of weights in (0, 1] (probabilities, fp32 exp terms) as 64.64
+// fixed-point integers: exact for every weight from 2^-40 up, and the
+// integer sum does not depend on the order of the terms.
+typedef unsigned __int128 u128;
+
+// w * 2^64 as an integer: exact for normal w >= 2^-40 (a 24-bit mantissa
+// shifted left), truncated below; 0 for w <= 0, subnormal or not below 2^40.
+__device__ __forceinline__ u128 to_fixed(float w) {
+  if (!(w > 0.f) || !(w < 1.0995116e12f)) return 0;
+  const uint32_t bits = __float_as_uint(w);
+  const int e = (int)((bits >> 23) & 255u);
+  if (e == 0) return 0;
+  const uint32_t mant = (bits & 0x7fffffu) | 0x800000u;
+  const int shift = e - 127 - 23 + 64;  // w = mant * 2^(e - 150)
+  if (shift >= 0) return (u128)mant << shift;
+  return shift > -24 ? (u128)(mant >> -shift) : (u128)0;
+}
+__device__ __forceinline__ double fixed_to_double(u128 m) {
+  return (double)(unsigned long long)(m >> 64) + ldexp((double)(unsigned long long)m, -64);
+}
+__device__ __forceinline__ u128 warp_sum_u128(u128 v) {
+#pragma unroll
+  for (int off = 16; off; off >>= 1) {
+    const unsigned long long lo = __shfl_xor_sync(0xffffffffu, (unsigned long long)v, off);
+    const unsigned long long hi = __shfl_xor_sync(0xffffffffu, (unsigned long long)(v >> 64), off);
+    v += ((u128)hi << 64) | lo;
+  }
+  return v;
+}
 // Order-preserving 32-bit key of an fp32 value: larger value -> larger key;
 // -0 and +0 share a key.  Truncation bounds are expressed in these keys.
 __device__ __forceinline__ uint32_t order_key(float f) {
