@@ -299,20 +299,28 @@ __global__ void __launch_bounds__(ACC_THREADS) accept_kernel(const AcceptParams 
 }
 
 // Row max / lowest argmax / sum-exp of raw fp32 logits (for callers that do
-// not pass the lm_head statistics).  One block per row.
+// not pass the lm_head statistics).  One thread-block cluster of up to 8 CTAs
+// per row, each a slice of it; the slices' results meet in distributed
+// shared memory (in slice order, so the lowest index of the maximum wins).
 __global__ void __launch_bounds__(1024) row_stats_kernel(const float* __restrict__ logits, int ldl, int V,
                                                          float temperature, float* row_max, float* row_sumexp,
                                                          int32_t* row_argmax) {
   pdl_trigger();
   pdl_wait();
-  const int r = blockIdx.x, tid = threadIdx.x;
+  const unsigned C = cluster_ctas(), rank = cluster_rank();
+  const int r = blockIdx.x / C, tid = threadIdx.x;
+  const int slice = (V + (int)C - 1) / (int)C;
+  const int v0 = min(V, (int)rank * slice), v1 = min(V, v0 + slice);
   const float* z = logits + (size_t)r * ldl;
   __shared__ float sb[1024];
   __shared__ int si[1024];
   __shared__ u128 sd[32];
+  __shared__ float cbest;
+  __shared__ int cidx;
+  __shared__ unsigned long long csum[2];
   float best = -INFINITY;
   int bi = 0x7fffffff;
-  for (int k = tid; k < V; k += 1024) {
+  for (int k = v0 + tid; k < v1; k += 1024) {
     const float v = z[k];
     if (v > best) { best = v; bi = k; }  // ascending k per thread: first maximum kept
   }
@@ -327,26 +335,45 @@ __global__ void __launch_bounds__(1024) row_stats_kernel(const float* __restrict
     }
     __syncthreads();
   }
-  best = sb[0];
-  bi = si[0];
+  if (tid == 0) {
+    cbest = sb[0];
+    cidx = si[0];
+  }
+  cluster_sync();
+  best = -INFINITY;
+  bi = 0x7fffffff;
+  for (unsigned q = 0; q < C; ++q) {
+    const float ob = __uint_as_float(ld_peer_u32(peer(&cbest, q)));
+    const int oi = (int)ld_peer_u32(peer(&cidx, q));
+    if (ob > best || (ob == best && oi < bi)) { best = ob; bi = oi; }
+  }
   double se = 0.0;
   if (temperature > 0.f) {  // the fp32 exp terms summed exactly (fixed point)
     u128 acc = 0;
-    for (int k = tid; k < V; k += 1024) acc += to_fixed(exp_term((z[k] - best) / temperature));
+    for (int k = v0 + tid; k < v1; k += 1024) acc += to_fixed(exp_term((z[k] - best) / temperature));
     acc = warp_sum_u128(acc);
     if ((tid & 31) == 0) sd[tid >> 5] = acc;
     __syncthreads();
     if (tid == 0) {
       u128 t = 0;
       for (int w = 0; w < 32; ++w) t += sd[w];
+      csum[0] = (unsigned long long)t;
+      csum[1] = (unsigned long long)(t >> 64);
+    }
+    cluster_sync();
+    if (tid == 0) {
+      u128 t = 0;
+      for (unsigned q = 0; q < C; ++q)
+        t += ((u128)ld_peer_u64(peer(&csum[1], q)) << 64) + ld_peer_u64(peer(&csum[0], q));
       se = fixed_to_double(t);
     }
   }
-  if (tid == 0) {
+  if (rank == 0 && tid == 0) {
     row_max[r] = best;
     row_argmax[r] = bi;
     if (temperature > 0.f) row_sumexp[r] = (float)se;
   }
+  cluster_sync();  // no CTA leaves while another may still read its shared memory
 }
 
 // Philox-4x32-10 (Salmon et al., SC'11): multiply-xor rounds with a Weyl key schedule.
@@ -377,10 +404,40 @@ cudaError_t launch_accept(const AcceptParams& p, int B, cudaStream_t s) {
   return cudaLaunchKernelEx(&cfg, accept_kernel, p);
 }
 
+// CTAs per row for row_stats_kernel: the largest cluster of up to 8 the device can place.
+static int row_stats_cluster() {
+  static int cached = 0;
+  if (cached) return cached;
+  int c = 8;
+  for (; c > 1; c >>= 1) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(c);
+    cfg.blockDim = dim3(1024);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = c;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, row_stats_kernel, &cfg) == cudaSuccess && n > 0) break;
+    cudaGetLastError();  // clear a refusal; try a smaller cluster
+  }
+  cached = c;
+  return c;
+}
+
 cudaError_t launch_row_stats(const float* logits, int ldl, int rows, int V, float temperature, float* row_max,
                              float* row_sumexp, int32_t* row_argmax, cudaStream_t s) {
-  cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = pdl_config(dim3(rows), dim3(1024), 0, s, attr);
+  const int c = row_stats_cluster();
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = pdl_config(dim3(rows * c), dim3(1024), 0, s, attr);
+  attr[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;
+  attr[cfg.numAttrs].val.clusterDim.x = c;
+  attr[cfg.numAttrs].val.clusterDim.y = 1;
+  attr[cfg.numAttrs].val.clusterDim.z = 1;
+  ++cfg.numAttrs;
   return cudaLaunchKernelEx(&cfg, row_stats_kernel, logits, ldl, V, temperature, row_max, row_sumexp, row_argmax);
 }
 

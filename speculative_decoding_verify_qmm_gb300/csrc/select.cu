@@ -61,39 +61,6 @@ struct SelShared {
   int top_idx[32];
 };
 
-// ------------------------------------------------------------- cluster plumbing
-__device__ __forceinline__ unsigned cluster_rank() {
-  unsigned r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ unsigned cluster_ctas() {
-  unsigned n;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
-  return n;
-}
-// Every thread of every CTA of the cluster; orders shared-memory writes before it
-// with the other CTAs' reads after it.
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// Shared-memory address of `p` in CTA `rank` of this cluster.
-__device__ __forceinline__ uint32_t peer(const void* p, unsigned rank) {
-  uint32_t a;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
-  return a;
-}
-__device__ __forceinline__ unsigned ld_peer_u32(uint32_t a) {
-  unsigned v;
-  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
-  return v;
-}
-__device__ __forceinline__ unsigned long long ld_peer_u64(uint32_t a) {
-  unsigned long long v;
-  asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(a) : "memory");
-  return v;
-}
-
 // Per-warp histograms (dynamic shared memory): counts, and masses as 64.64
 // fixed point split into the fraction word and the integer word.
 struct SelHist {

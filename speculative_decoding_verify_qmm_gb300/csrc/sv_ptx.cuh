@@ -176,6 +176,39 @@ __device__ __forceinline__ int ld_acquire_cta(const int* addr) {
 // Order this thread's generic-proxy global writes before later async-proxy (bulk copy) reads.
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
+// ------------------------------------------------------------- thread-block clusters
+__device__ __forceinline__ unsigned cluster_rank() {
+  unsigned r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ unsigned cluster_ctas() {
+  unsigned n;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
+  return n;
+}
+// Every thread of every CTA of the cluster; orders shared-memory writes before it
+// with the other CTAs' reads after it.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Shared-memory address of `p` in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t peer(const void* p, unsigned rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
+  return a;
+}
+__device__ __forceinline__ unsigned ld_peer_u32(uint32_t a) {
+  unsigned v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned long long ld_peer_u64(uint32_t a) {
+  unsigned long long v;
+  asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(a) : "memory");
+  return v;
+}
+
 // exp(x) for x <= 0 as a term of a softmax sum or a draw weight (the maximum
 // term is 1): x <= -87 gives 0 instead of a result below 1.2e-38, which keeps
 // expf (and anything dividing its result) off the subnormal slow paths.
