@@ -140,3 +140,36 @@ def test_rejections(lib):
         lib.truncate_probs(z, 0, 0.0)
     with pytest.raises(SVError):
         lib.logprobs(z, 1.0, top_n=33)
+
+
+@pytest.mark.parametrize("V", [1, 2, 5, 9, 17])
+def test_tiny_vocabularies_leave_slices_empty(lib, V):
+    """A row is split over up to 8 CTAs: vocabularies this small leave some of
+    them an empty slice (or a single token), which every call must get right."""
+    r = synthetic.rng(760 + V)
+    rows = 3
+    q = scipy.special.softmax(r.standard_normal((rows, V)) * 2.0, axis=1).astype(np.float32)
+    for top_k, top_p in [(0, 0.7), (2, 1.0), (3, 0.5), (0, 1.0)]:
+        got = lib.truncate_probs(torch.from_numpy(q).cuda(), top_k, top_p).cpu().numpy()
+        for i in range(rows):
+            if _boundary_near_tie(q[i], q[i].astype(np.float64), top_k, top_p, 1e-9):
+                continue
+            want = oa.truncate_probs(q[i], top_k, top_p)
+            assert np.array_equal(got[i] > 0, want > 0), (V, top_k, top_p, i)
+            assert np.allclose(got[i], want, rtol=2e-6, atol=1e-12)
+    z = (r.standard_normal((rows, V)) * 2.0).astype(np.float32)
+    chosen = r.integers(0, V, rows).astype(np.int32)
+    top_n = min(V, 8)
+    clp, ids, tlp = lib.logprobs(torch.from_numpy(z).cuda(), 0.9, chosen=torch.from_numpy(chosen).cuda(), top_n=top_n)
+    torch.cuda.synchronize()
+    clp, ids, tlp = clp.cpu().numpy(), ids.cpu().numpy(), tlp.cpu().numpy()
+    for i in range(rows):
+        w_lp, w_ids, w_top = oa.logprobs(z[i], 0.9, int(chosen[i]), top_n)
+        assert abs(clp[i] - w_lp) <= 1e-5 * max(1.0, abs(w_lp))
+        assert list(ids[i]) == list(w_ids)
+        assert np.all(np.abs(tlp[i] - w_top) <= 1e-5 * np.maximum(1.0, np.abs(w_top)))
+    if V >= 2:  # the truncated accept on the same small rows (m = 1)
+        got, det, exempt = _accept_case(lib, r, V, 1, 0.8, 2, 0.9)
+        if not exempt:
+            assert got == (det["out_len"], det["tokens"])
+    assert lib.device_error() == 0
