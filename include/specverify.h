@@ -71,6 +71,14 @@ int sv_version(void);
  * Returns SV_OK if no kernel recorded an error, SV_ETIMEOUT otherwise (the
  * raw bits go to *bits when bits != NULL), SV_ECUDA if the device call fails. */
 int sv_device_error(unsigned int* bits);
+/* Self-test of that path (no counterpart on the pages: a failure-detection
+ * check).  Enqueues on `stream` one device-side bounded wait on a barrier
+ * that nothing completes, limited to limit_us microseconds (1 .. 1e6); when it
+ * runs out the kernel records a timeout bit, exactly as the library's own
+ * waits do, and returns: the device faults nothing and stays usable.  The
+ * next sv_device_error() then returns SV_ETIMEOUT.  SV_EINVAL for a limit
+ * out of range. */
+int sv_selftest_bounded_wait(unsigned int limit_us, void* stream);
 
 /* ------------------------------------------------------------------ qmm ---
  * Y[m, n] = sum_k X[m, k] * w[n, k] for one verify projection

@@ -65,6 +65,7 @@ _SIGNATURES = {
     "sv_last_error": (ctypes.c_char_p, []),
     "sv_version": (_c_int, []),
     "sv_device_error": (_c_int, [_c_uint_p]),
+    "sv_selftest_bounded_wait": (_c_int, [ctypes.c_uint, _c_void_p]),
     "sv_qmm_workspace_bytes": (_c_size_t, [_c_int, _c_int, _c_int, _c_int]),
     "sv_qmm_verify": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_int, _c_int, _c_int, _c_int, _c_void_p, _c_int,
                                _c_int, _c_void_p, _c_int, _c_void_p, _c_int, _c_void_p, _c_size_t, _c_void_p]),

@@ -443,6 +443,13 @@ const char* sv_last_error(void) { return g_last; }
 
 int sv_version(void) { return 100; }
 
+int sv_selftest_bounded_wait(unsigned int limit_us, void* stream) {
+  if (limit_us < 1 || limit_us > 1000000u) return fail(SV_EINVAL, "limit_us must be in [1, 1e6] (got %u)", limit_us);
+  cudaError_t e = launch_wait_selftest(limit_us, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+  return SV_OK;
+}
+
 int sv_device_error(unsigned int* bits) {
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");

@@ -74,4 +74,27 @@ cudaError_t launch_swiglu(const __nv_bfloat16* g, int ldg, const __nv_bfloat16* 
   return cudaLaunchKernelEx(&cfg, swiglu_kernel, g, ldg, u, ldu, I, out, lds);
 }
 
+// Self-test of the bounded-wait error path: one thread waits on an mbarrier
+// that nothing arrives at, for at most limit_ns, and records the timeout in
+// the device error word as the library's own waits do (no fault, no trap).
+__global__ void wait_selftest_kernel(unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned long long t0 = global_ns();
+    bool done = mbar_try_wait(&bar, 0);
+    while (!done && global_ns() - t0 < limit_ns) done = mbar_try_wait(&bar, 0);
+    if (!done) raise_error(ERR_TIMEOUT_FULL);
+  }
+}
+
+cudaError_t launch_wait_selftest(unsigned int limit_us, cudaStream_t s) {
+  wait_selftest_kernel<<<1, 32, 0, s>>>((unsigned long long)limit_us * 1000ull);
+  return cudaGetLastError();
+}
+
 }  // namespace sv

@@ -56,6 +56,7 @@ struct SelectArgs {
   const int32_t* chosen; float* chosen_lp; int32_t* top_ids; float* top_lp; int top_n;  // SEL_TOPN
 };
 cudaError_t launch_select(const SelectArgs& a, int rows, cudaStream_t s);
+cudaError_t launch_wait_selftest(unsigned int limit_us, cudaStream_t s);
 
 struct AcceptParams {
   int offs[MAX_BATCH + 1];   // logits-row offsets of the requests (copied by value)
