@@ -607,7 +607,8 @@ def accept_variants(lib, steps, warmup, hbm):
 
 
 # ---------------------------------------------------------- CPU oracle leg
-SAMPLE_ROWS = 256
+SAMPLE_ROWS = 4096       # per projection in the round sample (about 1.5 s of all-core CPU work)
+PROJ_SAMPLE_ROWS = 256   # per single projection, at each of its row counts
 
 
 def oracle_sample(shape, M, temperature, seed=7):
@@ -655,7 +656,7 @@ def oracle_sample(shape, M, temperature, seed=7):
 
 
 def oracle_projection_sample(reps=3, seed=11):
-    """The CPU oracle's qmm_verify on SAMPLE_ROWS weight rows of each single
+    """The CPU oracle's qmm_verify on PROJ_SAMPLE_ROWS weight rows of each single
     projection, at every row count of PROJ_SHAPES, scaled to the projection's
     N rows: estimated µs per call (median of `reps`)."""
     import numpy as np
@@ -665,7 +666,7 @@ def oracle_projection_sample(reps=3, seed=11):
     out = {}
     for name, (N, K, bits, Ms) in PROJ_SHAPES.items():
         stats = synthetic.LARGE_8BIT if bits == 8 else synthetic.TINY_4BIT
-        R = min(SAMPLE_ROWS, N)
+        R = min(PROJ_SAMPLE_ROWS, N)
         w = synthetic.quant_weight(r, R, K, bits, stats)
         res = {}
         for M in Ms:
@@ -705,10 +706,11 @@ def cpu_baseline(M, reps):
     with the BLAS thread count set before numpy loads)."""
     out = {}
     ncpu = os.cpu_count() or 1
-    for label, threads in (("single_core", 1), ("all_cores", ncpu)):
+    # one timed sample on one core (several seconds), `reps` on all cores
+    for label, threads, n in (("single_core", 1, 1), ("all_cores", ncpu, reps)):
         env = dict(os.environ, OPENBLAS_NUM_THREADS=str(threads), OMP_NUM_THREADS=str(threads),
                    MKL_NUM_THREADS=str(threads), CUDA_VISIBLE_DEVICES="")
-        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-sample", "--reps", str(reps),
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-sample", "--reps", str(n),
                             "--only-m", str(M)], env=env, capture_output=True, text=True, timeout=900)
         if r.returncode != 0:
             out[label] = {"error": r.stderr[-400:]}
@@ -722,7 +724,7 @@ def cpu_baseline(M, reps):
                        env=env, capture_output=True, text=True, timeout=900)
     out["projections_single_core"] = (
         {"us_per_call": json.loads(r.stdout.strip().splitlines()[-1]), "cores": 1,
-         "sample": "%d weight rows of each projection, scaled to its N rows; median of 3" % SAMPLE_ROWS}
+         "sample": "%d weight rows of each projection, scaled to its N rows; median of 3" % PROJ_SAMPLE_ROWS}
         if r.returncode == 0 else {"error": r.stderr[-400:]})
     return out
 
