@@ -231,9 +231,10 @@ def kernel_roofline(rnd, reps):
 def e2e_rounds(rnd, steps):
     """Host buffers in, host result out, through the public call: each step
     copies the round's inputs in from pinned host memory (the hidden rows on
-    the round's stream; q, drafts and uniforms on a second stream, which the
-    accept step waits for through accept_wait_event, so that copy overlaps
-    the projections), runs the round, and reads out_len / out_tokens back;
+    the round's stream; q, drafts and uniforms on a second stream after them,
+    which the accept step waits for through accept_wait_event, so that copy
+    overlaps the projections), runs the round, whose accept step writes
+    out_len / out_tokens straight into pinned host memory, and waits for it;
     wall clock per round.  The copies and the round are one CUDA graph."""
     import torch
     host = [t.cpu().pin_memory() for t in (rnd.h0, rnd.q, rnd.draft, rnd.u)]
@@ -253,7 +254,7 @@ def e2e_rounds(rnd, steps):
                 dev.copy_(h, non_blocking=True)
             ready.record(side)
         with torch.cuda.stream(main):
-            rnd.lib.verify_round(rnd.model, rnd.offs, rnd.hidden, rnd.T, rnd.logits, rnd.out_len, rnd.out_tokens,
+            rnd.lib.verify_round(rnd.model, rnd.offs, rnd.hidden, rnd.T, rnd.logits, len_host, tok_host,
                                  rnd.ws, q=rnd.q, draft=rnd.draft, u=rnd.u, stream=main, accept_wait=ready)
 
     main.wait_stream(torch.cuda.current_stream())
@@ -267,10 +268,11 @@ def e2e_rounds(rnd, steps):
     for _ in range(steps):
         with torch.cuda.stream(main):
             g.replay()
-            len_host.copy_(rnd.out_len, non_blocking=True)
-            tok_host.copy_(rnd.out_tokens, non_blocking=True)
         main.synchronize()
-    return (time.perf_counter() - t0) * 1e6 / steps, h2d, d2h
+    us = (time.perf_counter() - t0) * 1e6 / steps
+    if not (0 < int(len_host[0]) <= rnd.out_tokens.numel()):
+        raise SystemExit("end-to-end round left no result in host memory")
+    return us, h2d, d2h
 
 
 def device_model(lib, seed, shape, stats, packed=True):

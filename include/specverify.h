@@ -314,7 +314,11 @@ int sv_swiglu(const uint16_t* g, int ldg, const uint16_t* u, int ldu, int M, int
  *   temperature, q (fp32, stride ldq), draft (int32), u (fp32): as in
  *     sv_spec_accept_batched.
  *   logits  fp32 [M, vocab] (stride ldl): the round's target logits.
- *   out_len int32 [B], out_tokens int32 [M]: the accept result.
+ *   out_len int32 [B], out_tokens int32 [M]: the accept result.  These two
+ *     may also be pinned host memory that the device can address (as from
+ *     cudaHostAlloc on a system with unified addressing): the accept step
+ *     then writes the result straight to the host, with no copy to order
+ *     after the round.
  *   event_start, event_stop: optional cudaEvent_t (NULL to skip) recorded on
  *     `stream` just before and after the launch that runs all the projections,
  *     for timing it (recording them adds a dependency that delays that launch

@@ -176,6 +176,52 @@ def test_round_accept_inputs_on_a_side_stream(lib):
     assert lib.device_error() == 0
 
 
+
+def test_round_writes_its_result_to_pinned_host_memory(lib):
+    """out_len / out_tokens in pinned host memory the device can address: the
+    accept step writes the result to the host directly, eagerly and from a
+    captured graph, with the same values as device outputs."""
+    layers, head = _model.host_model(1510, 2, bits=8, stats=synthetic.LARGE_8BIT, **TINY)
+    model = lib.make_model(_model.device_layers(layers), _model.to_device(head), TINY["hidden"], TINY["q_dim"],
+                           TINY["inter"], TINY["vocab"], 8)
+    r = synthetic.rng(1511)
+    m, B = 5, 2
+    M = B * (m + 1)
+    offs = [0, m + 1, M]
+    h0 = synthetic.activations(r, M, TINY["hidden"])
+    qn = np.concatenate([synthetic.logits_and_draft_probs(r, m, TINY["vocab"])[1] for _ in range(B)])
+    dn = synthetic.sample_drafts(r, qn)
+    un = synthetic.accept_uniforms(r, M)
+    q, d, u = (torch.from_numpy(a).cuda() for a in (qn, dn, un))
+    ref = _round(lib, model, offs, dev_bf16(h0), 1.0, q=q, draft=d, u=u)
+    hidden, h_init = dev_bf16(h0), dev_bf16(h0)
+    logits = torch.empty((M, TINY["vocab"]), dtype=torch.float32, device="cuda")
+    out_len = torch.zeros(B, dtype=torch.int32).pin_memory()
+    out_tokens = torch.full((M,), -1, dtype=torch.int32).pin_memory()
+    ws = lib.workspace(lib.round_workspace_bytes(model, M))
+    lib.verify_round(model, offs, hidden, 1.0, logits, out_len, out_tokens, ws, q=q, draft=d, u=u)
+    torch.cuda.synchronize()
+    assert (out_len.numpy() == ref[2]).all()
+    for b in range(B):  # each request's committed tokens (entries past out_len are untouched)
+        n = int(ref[2][b])
+        assert (out_tokens.numpy()[offs[b]:offs[b] + n] == ref[3][offs[b]:offs[b] + n]).all()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s), torch.cuda.graph(g, stream=s):
+        hidden.copy_(h_init)
+        lib.verify_round(model, offs, hidden, 1.0, logits, out_len, out_tokens, ws, q=q, draft=d, u=u, stream=s)
+    torch.cuda.synchronize()
+    out_len.zero_()
+    out_tokens.fill_(-1)
+    g.replay()
+    torch.cuda.synchronize()
+    assert (out_len.numpy() == ref[2]).all()
+    for b in range(B):
+        n = int(ref[2][b])
+        assert (out_tokens.numpy()[offs[b]:offs[b] + n] == ref[3][offs[b]:offs[b] + n]).all()
+    assert lib.device_error() == 0
+
 def _unpack_host(packed, N, K, bits):
     """Canonical (codes bytes [N, K*bits/8], scales, biases) read back from a unit-packed buffer,
     following the layout sv_qmm_pack documents: per (tile, chunk) unit, 128-byte pieces x 64 rows
