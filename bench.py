@@ -174,6 +174,17 @@ class Round:
         self.graph.replay()
 
 
+def max_over_ranks(v, dist=None, device="cuda"):
+    """The largest of a per-rank value over all ranks (the slowest replica sets
+    the job's time); v itself when there is no process group."""
+    if not dist:
+        return v
+    import torch
+    x = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    dist.all_reduce(x, op=dist.ReduceOp.MAX)
+    return float(x.item())
+
+
 def time_replays(fn, steps, warmup, dist=None):
     """µs of each of `steps` back-to-back calls, CUDA events between them on the current stream."""
     import torch
@@ -830,14 +841,7 @@ def main():
     if err:
         raise SystemExit("device error word 0x%x after the timed rounds" % err)
 
-    def max_over_ranks(v):
-        if not dist:
-            return v
-        x = torch.tensor([v], dtype=torch.float64, device="cuda")
-        dist.all_reduce(x, op=dist.ReduceOp.MAX)
-        return float(x.item())
-
-    us = {k: max_over_ranks(v) for k, v in t.items()}
+    us = {k: max_over_ranks(v, dist) for k, v in t.items()}
     gbs = {k: wbytes / (v * 1e-6) / 1e9 for k, v in us.items()}
     spreads = {str(Mx): spread(time_replays(rounds[Mx].replay, 100, 3)) for Mx in ms}
 
