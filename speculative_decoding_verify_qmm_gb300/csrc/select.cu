@@ -50,10 +50,9 @@ struct SelShared {
   int bin;
   double above;
   double total;
-  int ifound;
   // this CTA's values that the other CTAs of the cluster read (one slot per use)
   float cmax;
-  unsigned long long csum[4][2];  // exact sums: fraction word, integer word
+  unsigned long long csum[2][2];  // exact sums (kept mass, log-sum): fraction word, integer word
   int ccount[2];                  // tied keys in this slice, per tie search
   int cfound[2];                  // the tie index if it lies in this slice, else INT_MAX
   int n_top;
