@@ -15,9 +15,15 @@
 // activations, prepared once as fp16 scaled by a power of two per row (exact
 // for every bf16 value; the scale is undone in the epilogue).
 //
-// Arithmetic: w = fp16(fp32(fp32(scale * code) + bias)) - the oracle's fp32
-// weight, rounded once more to fp16 (relative error <= 2^-11) - times the exact
-// fp16 activations, fp32 accumulation.  When a projection has too few 128-row
+// Arithmetic: w = fp16(scale * code + bias) - one fused fp16 multiply-add of
+// the exact code, so within half an fp16 ulp (relative 2^-11) of the exact
+// affine weight and of the oracle's fp32 weight - times the exact fp16
+// activations, fp32 accumulation.  A 32-bit word of W = 32 / bits codes is
+// dequantized as the pairs (c_j, c_j+W/2): each is one mask of the shifted word
+// OR'ed into the mantissa of 1024 (fp16 1024 + c, exact), one subtraction of
+// 1024 and one fused multiply-add, two weights per instruction.  The weight
+// row's k order inside each word is then 0, W/2, 1, W/2+1, ...; the prepared
+// activations are stored in the same order, so the contraction is unchanged.  When a projection has too few 128-row
 // tiles to fill the GPU, k is split across CTAs and a second kernel adds the
 // fp32 partials in split order.
 #include <cstring>
@@ -52,11 +58,19 @@ struct WideParams {
 __host__ __device__ inline int wide_x_off() { return WT * 128; }
 __host__ __device__ inline int wide_codes_off(int rows) { return WT * 128 + rows * 128; }
 
+// The W / 2 weight pairs (c_j, c_j+W/2) of one code word, W = 32 / BITS,
+// as fp16 s * c + b.
 template <int BITS>
-__device__ __forceinline__ uint32_t code_at(const uint8_t* row, int k) {
-  if (BITS == 8) return row[k];
-  if (BITS == 4) return (row[k >> 1] >> ((k & 1) * 4)) & 15u;
-  return (row[k >> 2] >> ((k & 3) * 2)) & 3u;
+__device__ __forceinline__ void dequant_word(uint32_t w, __half2 s2, __half2 b2, uint32_t* out) {
+  constexpr uint32_t MASK = BITS == 8 ? 0x00ff00ffu : (BITS == 4 ? 0x000f000fu : 0x00030003u);
+  const __half2 k1024 = __half2half2(__ushort_as_half((unsigned short)0x6400));
+#pragma unroll
+  for (int j = 0; j < 16 / BITS; ++j) {
+    const uint32_t biased = ((w >> (BITS * j)) & MASK) | 0x64006400u;  // fp16 1024 + c in each half
+    const __half2 c2 = __hsub2(*reinterpret_cast<const __half2*>(&biased), k1024);
+    const __half2 w2 = __hfma2(s2, c2, b2);
+    out[j] = *reinterpret_cast<const uint32_t*>(&w2);
+  }
 }
 
 template <int BITS>
@@ -80,7 +94,7 @@ __global__ void __launch_bounds__(W_THREADS, 1) wide_kernel(const __grid_constan
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full_bar[s], 1);
-      mbar_init(&deq_bar[s], W_DQ * 32);
+      mbar_init(&deq_bar[s], W_DQ);  // one arrival per dequantizing warp
       mbar_init(&empty_bar[s], 1);
     }
     mbar_init(&acc_bar, 1);
@@ -165,10 +179,13 @@ __global__ void __launch_bounds__(W_THREADS, 1) wide_kernel(const __grid_constan
     // thread t: weight row r = t % 128 of the tile, k half h = t / 128 (32 codes)
     const int r = threadIdx.x & (WT - 1), h = threadIdx.x / WT;
     constexpr int HB = WK * BITS / 16;  // code bytes of half a row's k-step
+    constexpr int PW = 16 / BITS;       // weight pairs per code word
     for (int i = 0; i < nk; ++i) {
       const int s = i % S, ks = ks0 + i;
-      if (*abort_v) break;
-      if (!mbar_wait_bounded(&full_bar[s], (i / S) & 1, abort_v)) {
+      // the warp decides together: its arrival below is one per warp
+      bool ok = !*abort_v && mbar_wait_bounded(&full_bar[s], (i / S) & 1, abort_v);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) {
         if (!*abort_v) raise_error(ERR_TIMEOUT_FULL);
         *abort_v = 1;
         break;
@@ -177,32 +194,32 @@ __global__ void __launch_bounds__(W_THREADS, 1) wide_kernel(const __grid_constan
       const uint8_t* codes = st + wide_codes_off(p.chunk) + r * (WK * BITS / 8) + h * HB;
       const __half* sc = reinterpret_cast<const __half*>(st + wide_codes_off(p.chunk) + p.codes_bytes);
       const __half* bi = sc + WT * 8;
-      const float scale = __half2float(sc[r * 8 + (ks & 7)]);
-      const float bias = __half2float(bi[r * 8 + (ks & 7)]);
-      uint8_t local[HB < 16 ? 16 : HB];
-      if constexpr (HB >= 16) {
+      const __half2 s2 = __half2half2(sc[r * 8 + (ks & 7)]);
+      const __half2 b2 = __half2half2(bi[r * 8 + (ks & 7)]);
+      uint32_t words[BITS];  // the thread's 32 codes
+      if constexpr (BITS >= 4) {
 #pragma unroll
-        for (int j = 0; j < HB; j += 16)
-          *reinterpret_cast<uint4*>(local + j) = *reinterpret_cast<const uint4*>(codes + j);
+        for (int j = 0; j < BITS; j += 4) {
+          const uint4 v = *reinterpret_cast<const uint4*>(codes + 4 * j);
+          words[j] = v.x; words[j + 1] = v.y; words[j + 2] = v.z; words[j + 3] = v.w;
+        }
       } else {  // 2-bit: 8 bytes per half row
-        *reinterpret_cast<uint2*>(local) = *reinterpret_cast<const uint2*>(codes);
+        const uint2 v = *reinterpret_cast<const uint2*>(codes);
+        words[0] = v.x; words[1] = v.y;
       }
+      uint32_t pairs[16];
+#pragma unroll
+      for (int j = 0; j < BITS; ++j) dequant_word<BITS>(words[j], s2, b2, pairs + PW * j);
       uint8_t* arow = st + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
         const int c = 4 * h + cc;  // 16-byte chunk (8 fp16) of the row's 128 bytes
-        uint32_t packed[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float w0 = __fadd_rn(__fmul_rn(scale, (float)code_at<BITS>(local, 8 * cc + 2 * e)), bias);
-          const float w1 = __fadd_rn(__fmul_rn(scale, (float)code_at<BITS>(local, 8 * cc + 2 * e + 1)), bias);
-          const __half2 hw = __floats2half2_rn(w0, w1);
-          packed[e] = *reinterpret_cast<const uint32_t*>(&hw);
-        }
-        *reinterpret_cast<uint4*>(arow + ((c ^ (r & 7)) << 4)) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        *reinterpret_cast<uint4*>(arow + ((c ^ (r & 7)) << 4)) =
+            make_uint4(pairs[4 * cc], pairs[4 * cc + 1], pairs[4 * cc + 2], pairs[4 * cc + 3]);
       }
       fence_proxy_async_smem();  // the tensor cores read these writes through the async proxy
-      mbar_arrive(&deq_bar[s]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&deq_bar[s]);
     }
     // epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31 (weight rows), the
     // first half of the columns (block rows) for w < 4, the second for w >= 4
@@ -245,9 +262,11 @@ __global__ void __launch_bounds__(W_THREADS, 1) wide_kernel(const __grid_constan
 }
 
 // Activations for the wide kernel: fp16 x * 2^e per row (e = 15 - exponent of
-// the row's max |x|), 2^-e per row; rows M .. Mpad-1 zero.  One block per row.
+// the row's max |x|), 2^-e per row; rows M .. Mpad-1 zero.  Inside each block of
+// W = 32 / bits k (one code word) the values are stored in the dequantized
+// weights' order: position q holds k = q / 2 + (q % 2) * W / 2.  One block per row.
 __global__ void __launch_bounds__(256) wide_prep_kernel(const __nv_bfloat16* __restrict__ x, int ldx, int M, int K,
-                                                        __half* __restrict__ x16, float* __restrict__ inv) {
+                                                        int bits, __half* __restrict__ x16, float* __restrict__ inv) {
   pdl_trigger();
   pdl_wait();
   const int m = blockIdx.x, tid = threadIdx.x;
@@ -262,8 +281,11 @@ __global__ void __launch_bounds__(256) wide_prep_kernel(const __nv_bfloat16* __r
   for (int w = 0; w < 8; ++w) mx = fmaxf(mx, s_max[w]);
   const int e = scale_exponent(mx);
   const float sc = pow2_exact(e);
-  for (int k = tid; k < K; k += 256)
-    x16[(size_t)m * K + k] = __float2half_rn(m < M ? __bfloat162float(x[(size_t)m * ldx + k]) * sc : 0.f);
+  const int W = 32 / bits;
+  for (int q = tid; q < K; q += 256) {
+    const int k = (q & ~(W - 1)) + ((q & (W - 1)) >> 1) + (q & 1) * (W / 2);
+    x16[(size_t)m * K + q] = __float2half_rn(m < M ? __bfloat162float(x[(size_t)m * ldx + k]) * sc : 0.f);
+  }
   if (tid == 0) inv[m] = pow2_exact(-e);
 }
 
@@ -388,7 +410,7 @@ int wide_qmm(const uint32_t* wq, const uint16_t* scales, const uint16_t* biases,
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = pdl_config(dim3(w.Mpad), dim3(256), 0, s, attr);
     cudaError_t e = cudaLaunchKernelEx(&cfg, wide_prep_kernel, reinterpret_cast<const __nv_bfloat16*>(x), ldx, M, K,
-                                       x16, inv);
+                                       bits, x16, inv);
     if (e != cudaSuccess) return cuda_fail(e, "wide preparation launch");
   }
   static thread_local WideParams p;
