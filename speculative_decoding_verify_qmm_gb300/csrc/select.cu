@@ -41,6 +41,10 @@ namespace sv {
 constexpr int SEL_THREADS = 1024;
 constexpr int SEL_WARPS = SEL_THREADS / 32;
 constexpr int SEL_MAX_CLUSTER = 8;  // CTAs per row (the portable cluster size)
+// Elements a thread loads before it updates the histograms: the loads of a
+// batch are independent and in flight together (loads interleaved with the
+// shared-memory atomics went out one L2 round trip after another).
+constexpr int SEL_BATCH = 4;
 
 struct SelShared {
   int cnt[256];          // the cluster's bin totals of the current pass
@@ -107,18 +111,27 @@ __device__ void radix_pass(const float* x, int v0, int v1, int shift, uint32_t p
     if (WITH_MASS) h.lo[wid][b] = h.hi[wid][b] = 0ull;
   }
   __syncwarp();
-  for (int v = v0 + tid; v < v1; v += SEL_THREADS) {
-    const float xv = x[v];
-    const uint32_t key = order_key(xv);
-    if ((key & pmask) != prefix || !keep(key, v)) continue;
-    const int b = (key >> shift) & 255;
-    atomicAdd(&h.cnt[wid][b], 1u);
-    if (WITH_MASS) {
-      const u128 wf = to_fixed(weight(xv));
-      const unsigned long long lo = (unsigned long long)wf, hi = (unsigned long long)(wf >> 64);
-      const unsigned long long old = atomicAdd(&h.lo[wid][b], lo);
-      const unsigned long long carry = old > ~lo ? 1ull : 0ull;  // this add wrapped the fraction word
-      if (hi | carry) atomicAdd(&h.hi[wid][b], hi + carry);
+  for (int vb = v0 + tid; vb < v1; vb += SEL_BATCH * SEL_THREADS) {
+    float xs[SEL_BATCH];
+#pragma unroll
+    for (int j = 0; j < SEL_BATCH; ++j) {
+      const int v = vb + j * SEL_THREADS;
+      xs[j] = v < v1 ? __ldg(x + v) : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < SEL_BATCH; ++j) {
+      const int v = vb + j * SEL_THREADS;
+      const uint32_t key = order_key(xs[j]);
+      if (v >= v1 || (key & pmask) != prefix || !keep(key, v)) continue;
+      const int b = (key >> shift) & 255;
+      atomicAdd(&h.cnt[wid][b], 1u);
+      if (WITH_MASS) {
+        const u128 wf = to_fixed(weight(xs[j]));
+        const unsigned long long lo = (unsigned long long)wf, hi = (unsigned long long)(wf >> 64);
+        const unsigned long long old = atomicAdd(&h.lo[wid][b], lo);
+        const unsigned long long carry = old > ~lo ? 1ull : 0ull;  // this add wrapped the fraction word
+        if (hi | carry) atomicAdd(&h.hi[wid][b], hi + carry);
+      }
     }
   }
   __syncthreads();
@@ -253,7 +266,13 @@ __device__ int tie_index(const float* x, int v0, int v1, uint32_t K, int limit, 
   const int per = (n + SEL_THREADS - 1) / SEL_THREADS;
   const int a = v0 + min(n, tid * per), e = v0 + min(n, tid * per + per);
   int c = 0;
-  for (int v = a; v < e; ++v) c += order_key(x[v]) == K;
+  for (int vb = a; vb < e; vb += SEL_BATCH) {
+    float xs[SEL_BATCH];
+#pragma unroll
+    for (int j = 0; j < SEL_BATCH; ++j) xs[j] = vb + j < e ? __ldg(x + vb + j) : 0.f;
+#pragma unroll
+    for (int j = 0; j < SEL_BATCH; ++j) c += vb + j < e && order_key(xs[j]) == K;
+  }
   int incl = c;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
