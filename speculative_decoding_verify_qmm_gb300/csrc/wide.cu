@@ -74,7 +74,7 @@ __device__ __forceinline__ void dequant_word(uint32_t w, __half2 s2, __half2 b2,
 }
 
 template <int BITS>
-__global__ void __launch_bounds__(W_THREADS, 1) wide_kernel(const __grid_constant__ WideParams p) {
+__global__ void __launch_bounds__(W_THREADS, 2) wide_kernel(const __grid_constant__ WideParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full_bar[W_MAX_STAGES], deq_bar[W_MAX_STAGES], empty_bar[W_MAX_STAGES], acc_bar, fin_bar;
   __shared__ uint32_t s_tmem;
@@ -227,27 +227,78 @@ __global__ void __launch_bounds__(W_THREADS, 1) wide_kernel(const __grid_constan
     ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld is warp-collective: the whole warp reads or none
     tc05_fence_after();
     const int lq = warp & 3;
-    const int n = n0 + 32 * lq + lane;
+    const int nb = n0 + 32 * lq;  // this warp's 32 weight rows (the lane's is nb + lane)
     const int split_col = (p.chunk / 32) * 16;  // a multiple of 16: the loads read 16 columns at a time
     const int col0 = (warp >> 2) ? split_col : 0, col1 = (warp >> 2) ? p.chunk : split_col;
+    // Scratch in the stage ring, idle once the accumulators are final (every
+    // copy has landed and every MMA has read its stage): per warp 4 KB, the
+    // row scales of its columns, then one 16 x 32 chunk in output order.
+    float* const s_inv = reinterpret_cast<float*>(smem + warp * 4096);
+    uint8_t* const s_buf = smem + warp * 4096 + 512;
+    const bool partial_out = p.splits > 1;
+    // 16-byte stores along an output row need aligned rows (and residual rows)
+    const bool vec = partial_out
+                         ? (p.N % 4 == 0)
+                         : (p.ldy % 8 == 0 && (reinterpret_cast<uintptr_t>(p.y) & 15) == 0 &&
+                            (!p.res || (p.ldr % 8 == 0 && (reinterpret_cast<uintptr_t>(p.res) & 15) == 0)));
     if (ok) {
+      for (int i = lane; i < col1 - col0; i += 32) {
+        const int m = m0 + col0 + i;
+        s_inv[i] = m < p.M ? p.inv_scale[m] : 0.f;
+      }
+      __syncwarp();
       for (int col = col0; col < col1; col += 16) {
         float v[16];
         tmem_ld16(tmem + ((uint32_t)(32 * lq) << 16) + (uint32_t)col, v);
+        const int mc = m0 + col;  // block row of column j: mc + j
+        if (partial_out) {
+          float* buf = reinterpret_cast<float*>(s_buf);  // [16][32]
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int m = m0 + col + j;
-          if (m < p.M && n < p.N) {
-            const float val = v[j] * p.inv_scale[m];
-            if (p.splits > 1) {
-              p.partials[((size_t)split * p.M + m) * p.N + n] = val;
+          for (int j = 0; j < 16; ++j) buf[j * 32 + lane] = v[j] * s_inv[col - col0 + j];
+          __syncwarp();
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const int q = lane + 32 * t, j = q >> 3, c = q & 7, m = mc + j, nn = nb + 4 * c;
+            if (m >= p.M) continue;
+            float* dst = p.partials + ((size_t)split * p.M + m) * p.N + nn;
+            if (vec && nn + 4 <= p.N) {
+              *reinterpret_cast<float4*>(dst) = *reinterpret_cast<const float4*>(buf + j * 32 + 4 * c);
             } else {
-              float out = __bfloat162float(__float2bfloat16_rn(val));
-              if (p.res) out = __bfloat162float(p.res[(size_t)m * p.ldr + n]) + out;
-              p.y[(size_t)m * p.ldy + n] = __float2bfloat16_rn(out);
+              for (int e = 0; e < 4 && nn + e < p.N; ++e) dst[e] = buf[j * 32 + 4 * c + e];
+            }
+          }
+        } else {
+          __nv_bfloat16* buf = reinterpret_cast<__nv_bfloat16*>(s_buf);  // [16][32]
+#pragma unroll
+          for (int j = 0; j < 16; ++j) buf[j * 32 + lane] = __float2bfloat16_rn(v[j] * s_inv[col - col0 + j]);
+          __syncwarp();
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const int q = lane + 32 * t, j = q >> 2, c = q & 3, m = mc + j, nn = nb + 8 * c;
+            if (m >= p.M) continue;
+            const __nv_bfloat16* src = buf + j * 32 + 8 * c;
+            __nv_bfloat16* dst = p.y + (size_t)m * p.ldy + nn;
+            if (vec && nn + 8 <= p.N) {
+              uint4 o = *reinterpret_cast<const uint4*>(src);
+              if (p.res) {  // y = bf16(residual + bf16(product)), element by element
+                const uint4 rr = *reinterpret_cast<const uint4*>(p.res + (size_t)m * p.ldr + nn);
+                const __nv_bfloat16* rb = reinterpret_cast<const __nv_bfloat16*>(&rr);
+                __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(&o);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                  ob[e] = __float2bfloat16_rn(__bfloat162float(rb[e]) + __bfloat162float(ob[e]));
+              }
+              *reinterpret_cast<uint4*>(dst) = o;
+            } else {
+              for (int e = 0; e < 8 && nn + e < p.N; ++e) {
+                float out = __bfloat162float(src[e]);
+                if (p.res) out = __bfloat162float(p.res[(size_t)m * p.ldr + nn + e]) + out;
+                dst[e] = __float2bfloat16_rn(out);
+              }
             }
           }
         }
+        __syncwarp();  // the chunk buffer is rewritten by the next chunk
       }
     } else if (!*abort_v) {
       raise_error(ERR_TIMEOUT_FULL);

@@ -44,6 +44,28 @@ def test_wide_small_shape_everywhere(lib, bits, M):
     assert lib.device_error() == 0
 
 
+@pytest.mark.parametrize("M", [40, 300])
+def test_wide_unaligned_output_rows(lib, M):
+    """N = 203: output rows that are not 16-byte aligned take the epilogue's
+    element-by-element stores (bf16 output and, with k split across CTAs,
+    the fp32 partials).  The product is checked against the oracle; the
+    residual form must equal bf16(residual + product) with the GPU's own
+    (deterministic) product, element for element."""
+    r = synthetic.rng(1970 + M)
+    N, K, bits = 203, 2048, 4
+    w = synthetic.quant_weight(r, N, K, bits, STATS[bits])
+    x = synthetic.activations(r, M, K)
+    res = synthetic.activations(r, M, N)
+    _check(lib, w, x, what="wide N=203 M=%d" % M)
+    dw = dev_weight(w)
+    prod = lib.qmm_verify(dw["wq"], dw["scales"], dw["biases"], K, bits, dev_bf16(x))
+    y = lib.qmm_verify(dw["wq"], dw["scales"], dw["biases"], K, bits, dev_bf16(x), residual=dev_bf16(res))
+    torch.cuda.synchronize()
+    want = quant.f32_to_bf16_bits(quant.bf16_bits_to_f32(res) + host_f32_of_bf16(prod))
+    assert np.array_equal(host_f32_of_bf16(y), quant.bf16_bits_to_f32(want))
+    assert lib.device_error() == 0
+
+
 SHAPES = {  # Qwen3-8B-shaped (8-bit) and 4B-shaped (4-bit) projections
     "8b_q": (4096, 4096, 8), "8b_gate": (12288, 4096, 8), "8b_down": (4096, 12288, 8),
     "4b_q": (4096, 2560, 4), "4b_o": (2560, 4096, 4), "4b_gate": (9728, 2560, 4), "4b_down": (2560, 9728, 4),
