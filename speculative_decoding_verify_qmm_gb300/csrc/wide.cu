@@ -379,13 +379,14 @@ static WidePlan wide_plan(int M, int N, int K, int bits, int sms) {
   // k-step of a CTA is a chain of a copy, barrier hops, the dequantizing and
   // the MMAs, and each wave of CTAs has a fixed part (pipeline fill,
   // tensor-memory set-up, epilogue):
-  //   waves x (k-steps x (0.57 + 0.72 / S + per_sm x (0.0005 rows - 0.009))
-  //            + 3.3 + 0.017 rows)
-  //   + for s > 1: 2.3e-6 x M x N x s (fp32 partials out and back) + 5.3.
-  // Least-squares fit to 256 forced plans (one or two CTAs per SM, 1-16
-  // splits; 8-bit gate|up, down and q and 4-bit gate|up and down shapes at 33,
-  // 64, 128, 256 and 512 rows): median error 5 %, and the plan it picks is
-  // the measured best or within 6 % of it for every shape and width.  Two
+  //   waves x (k-steps x (0.514 + 1.071 / S + per_sm x (0.000202 rows - 0.076))
+  //            + 3.57 - 0.00706 rows)
+  //   + for s > 1: 2.44e-6 x M x N x s (fp32 partials out and back) + 5.35.
+  // Least-squares fit (relative error) to 256 forced plans (one or two CTAs
+  // per SM, 1-16 splits; 8-bit gate|up, down and q and 4-bit gate|up and down
+  // shapes at 33, 64, 128, 256 and 512 rows): median error 5 %, and the plan
+  // it picks is the measured best or within 6 % of it for every shape and
+  // width (the picks' times sum to 1252 us against 1248 for the best).  Two
   // CTAs per SM (half the stages each, when their tensor memory and shared
   // memory fit) win when they put the grid in fewer waves, e.g. the 192
   // gate|up tiles at 64 rows: 103 us in two waves of one CTA per SM, 72 in one
@@ -403,12 +404,12 @@ static WidePlan wide_plan(int M, int N, int K, int bits, int sms) {
       if (st > W_MAX_STAGES) st = W_MAX_STAGES;
       if (st < 2 || per_sm * cols > 512) continue;
       const long long slots = (long long)sms * per_sm;
-      const double step_us = 0.57 + 0.72 / st + per_sm * (0.0005 * w.chunk - 0.009);
-      const double wave_us = 3.3 + 0.017 * w.chunk;
+      const double step_us = 0.514 + 1.071 / st + per_sm * (0.000202 * w.chunk - 0.076);
+      const double wave_us = 3.57 - 0.00706 * w.chunk;
       for (int sp = 1; sp <= max_split && sp <= 16; ++sp) {
         const double waves = (double)((items * (long long)sp + slots - 1) / slots);
         const double ksteps = (double)((w.ks_total + sp - 1) / sp);
-        const double partials_us = sp > 1 ? 2.3e-6 * M * (double)N * sp + 5.3 : 0.0;
+        const double partials_us = sp > 1 ? 2.44e-6 * M * (double)N * sp + 5.35 : 0.0;
         const double cost = waves * (ksteps * step_us + wave_us) + partials_us;
         if (cost < best * (1.0 - 1e-9)) {
           best = cost;
