@@ -381,17 +381,22 @@ __global__ void __launch_bounds__(SEL_THREADS) select_kernel(const SelectArgs p)
       __syncthreads();
     }
     K = prefix;
-    // every tied token has the same value, hence the same weight
-    float xk = 0.f;
-    {
+    // every tied token has the same value, hence the same weight; the tied
+    // tokens to keep and the kept mass are the same scalars for every thread,
+    // so one thread computes them (fp64, a divide) and shares them
+    if (tid == 0) {
       const uint32_t u = (K & 0x80000000u) ? (K & 0x7fffffffu) : ~K;
-      xk = __uint_as_float(u);
+      const double wt = fixed_to_double(to_fixed(weight(__uint_as_float(u))));
+      int r = wt > 0.0 ? (int)ceil((theta - above_total) / wt) : ties;
+      r = max(1, min(r, ties));
+      sh.bin = r;
+      sh.above = above_total + (double)r * wt;
     }
-    const double wt = fixed_to_double(to_fixed(weight(xk)));
-    int r = wt > 0.0 ? (int)ceil((theta - above_total) / wt) : ties;
-    r = max(1, min(r, ties));
+    __syncthreads();
+    const int r = sh.bin;
+    kept_mass = sh.above;
+    __syncthreads();
     I = tie_index(x, v0, v1, K, K == Kk ? Ik : V - 1, r, 1, C, rank, sh);
-    kept_mass = above_total + (double)r * wt;
   } else if (p.mode != SEL_TOPN) {
     u128 w = 0;
     for (int v = v0 + tid; v < v1; v += SEL_THREADS) {
@@ -409,7 +414,9 @@ __global__ void __launch_bounds__(SEL_THREADS) select_kernel(const SelectArgs p)
     }
   } else if (p.mode == SEL_PROBS) {
     float* y = p.y + (size_t)row * p.ldy;
-    const double inv = 1.0 / kept_mass;
+    if (tid == 0) sh.total = 1.0 / kept_mass;  // one fp64 divide, shared
+    __syncthreads();
+    const double inv = sh.total;
     for (int v = v0 + tid; v < v1; v += SEL_THREADS) {
       const float xv = x[v];
       const uint32_t key = order_key(xv);
@@ -419,7 +426,10 @@ __global__ void __launch_bounds__(SEL_THREADS) select_kernel(const SelectArgs p)
     // ---- SEL_TOPN: log-probabilities of the chosen token and of the top_n tokens
     u128 sx = 0;
     for (int v = v0 + tid; v < v1; v += SEL_THREADS) sx += to_fixed(exp_term((x[v] - xmax) / T));
-    const double log_s = log(cluster_sum_fixed(sx, 1, C, h, sh));
+    const double s_sum = cluster_sum_fixed(sx, 1, C, h, sh);
+    if (tid == 0) sh.above = log(s_sum);  // one fp64 log, shared
+    __syncthreads();
+    const double log_s = sh.above;
     if (p.top_n > 0) {
       // each CTA lists its slice's kept tokens (k_lim of them in the whole row, at most 32)
       if (tid == 0) sh.n_top = 0;
